@@ -1,0 +1,175 @@
+/*
+ * mg.h -- C ABI of the GB300 training-step library (libmg.so).
+ *
+ * One training step of a typed static graph -- forward pass, hand-derived
+ * backward pass and optimizer update -- on one GPU, behind a fixed-shape plan.
+ * The operation follows the Meganeura pages: "Meganeura" README, Example
+ * section (a graph of input / parameter / matmul / relu / cross_entropy_loss
+ * nodes, built once with build_session and stepped by a Trainer), Contents
+ * section (SGD, Adam), Environment variables section (strict f32 scalar matmul
+ * versus validated reduced-precision tiles); and the abstract of "Meganeura:
+ * Portable GPU Training and Inference through Vulkan and Metal" (typed static
+ * graph, automatic differentiation, optimizer, memory planner, runtime; strict
+ * f32 kept apart from validated fast paths).
+ *
+ * Conventions for every call:
+ *  - Pointers named params/grads/adam_m/adam_v/x/labels/out are DEVICE
+ *    pointers owned by the caller (e.g. from torch tensors) and must be
+ *    16-byte aligned.  The plan never frees them.
+ *  - Everything is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *    default stream) except mg_loss, which synchronises it.
+ *  - Every call returns an mg_status; nothing aborts, throws across the ABI or
+ *    traps on the device.  mg_last_error() returns the message of the last
+ *    failure (per plan, or process-wide for a NULL plan).
+ *  - A plan is bound to the CUDA device that was current at creation and is not
+ *    thread-safe: drive it from one host thread and one stream at a time.
+ */
+#ifndef MG_H
+#define MG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mg_plan mg_plan;          /* opaque; owns the workspace */
+typedef struct CUstream_st* mg_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MG_OK = 0,
+  MG_ERR_INVALID_ARG = -1, /* NULL where a pointer is required, bad enum, bad value */
+  MG_ERR_UNSUPPORTED = -2, /* a valid graph this library has no kernels for */
+  MG_ERR_SHAPE = -3,       /* widths that do not chain, batch not a multiple of seq_len */
+  MG_ERR_ALIGN = -4,       /* a pointer that is not 16-byte aligned */
+  MG_ERR_OOM = -5,         /* workspace allocation failed (nothing leaked) */
+  MG_ERR_CUDA = -6,        /* a CUDA runtime/driver error (launch or earlier async fault) */
+  MG_ERR_NONFINITE = -7,   /* mg_debug_check_finite found a NaN or Inf */
+  MG_ERR_TIMEOUT = -8,     /* a bounded device-side wait gave up */
+  MG_ERR_INTERNAL = -9
+} mg_status;
+
+typedef enum {
+  MG_OP_LINEAR = 0,           /* Y = X W (+ b), W[d_in, d_out] row-major, b[d_out] */
+  MG_OP_RELU = 1,             /* max(z, 0); derivative 0 at z = 0 */
+  MG_OP_GELU_TANH = 2,        /* 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3))) */
+  MG_OP_RMSNORM = 3,          /* y = x / sqrt(mean(x^2) + eps) * gamma, gamma[d] */
+  MG_OP_RESIDUAL_BEGIN = 4,   /* remember the current value as the skip input */
+  MG_OP_RESIDUAL_END = 5,     /* value = skip + value */
+  MG_OP_CAUSAL_ATTENTION = 6  /* input [rows, 3d] = [Q|K|V], output [rows, d], d = n_heads*head_dim */
+} mg_op;
+
+typedef enum { MG_LOSS_CE_DENSE = 0, MG_LOSS_CE_INDEX = 1, MG_LOSS_MSE = 2 } mg_loss_kind;
+typedef enum { MG_PREC_STRICT_F32 = 0, MG_PREC_BF16 = 1 } mg_precision;
+typedef enum { MG_OPT_SGD = 0, MG_OPT_ADAM = 1 } mg_optimizer;
+
+typedef struct {
+  int op;        /* mg_op */
+  int d_in;      /* LINEAR: input width; RMSNORM: width */
+  int d_out;     /* LINEAR: output width */
+  int has_bias;  /* LINEAR: 1 if a bias vector follows W in the parameters */
+  float eps;     /* RMSNORM: epsilon inside the square root */
+  int n_heads;   /* CAUSAL_ATTENTION */
+  int head_dim;  /* CAUSAL_ATTENTION (64 supported) */
+  int seq_len;   /* CAUSAL_ATTENTION: rows are [batch, seq_len] flattened */
+} mg_layer;
+
+typedef struct {
+  int batch;               /* rows of x (tokens) */
+  int n_layers;
+  const mg_layer* layers;  /* copied at creation */
+  int loss;                /* mg_loss_kind, applied to the last layer's output */
+  int precision;           /* mg_precision */
+  int optimizer;           /* mg_optimizer */
+  float beta1, beta2, adam_eps;
+} mg_graph_desc;
+
+/* Build a plan for the current CUDA device: validate the descriptor, assign
+ * parameter offsets, choose a kernel per GEMM, allocate the workspace once.
+ * On failure *out is set to NULL and nothing is leaked.  The descriptor is the
+ * typed static graph of the README's Example section, with its shapes fixed. */
+mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out);
+
+/* Free the workspace.  NULL is a no-op.  Synchronises the device first. */
+void mg_step_plan_destroy(mg_plan* plan);
+
+/* Floats in each of the flat parameter / gradient / moment buffers. */
+size_t mg_param_count(const mg_plan* plan);
+
+/* Number of parameter tensors (W, b, gamma in declaration order). */
+int mg_param_tensor_count(const mg_plan* plan);
+
+/* Tensor i of the flat buffers: element offset, logical rows and cols (a
+ * vector has rows = 1).  Offsets are multiples of 64 elements; the gaps
+ * between tensors are never read or written. */
+mg_status mg_param_info(const mg_plan* plan, int i, size_t* offset, int* rows, int* cols);
+
+/* Bytes of device workspace the plan owns. */
+size_t mg_workspace_bytes(const mg_plan* plan);
+
+/* Forward pass only.  params: flat fp32 [mg_param_count]; x: [batch, d_in],
+ * fp32 in strict mode, bf16 in bf16 mode; out: fp32 [batch, d_out] (logits or
+ * the model output), written row-major. */
+mg_status mg_forward(mg_plan* plan, const float* params, const void* x, float* out,
+                     mg_stream_t stream);
+
+/* One full training step: forward, loss, backward, optimizer update.
+ *  params  fp32 [P]  updated in place (fp32 master weights)
+ *  grads   fp32 [P]  overwritten with dLoss/dparams of this step (before the update)
+ *  adam_m, adam_v fp32 [P]  Adam moments, updated in place; may be NULL under SGD
+ *  x       [batch, d_in], fp32 (strict) or bf16 (bf16)
+ *  labels  CE_DENSE: fp32 [batch, C]; CE_INDEX: int32 [batch], values in [0, C);
+ *          MSE: target [batch, d_out] in the activation dtype (fp32 / bf16)
+ *  lr      learning rate; step: Adam's t, 1-based (ignored by SGD)
+ * The loss of the step is kept on the device (mg_loss, mg_loss_device_ptr).
+ * grads must not alias params.  The bf16 weight copy used by the bf16 path is
+ * refreshed from params automatically when step == 1 or params differs from the
+ * previous call; otherwise the previous update has kept it current. */
+mg_status mg_train_step(mg_plan* plan, float* params, float* grads, float* adam_m,
+                        float* adam_v, const void* x, const void* labels, float lr, int step,
+                        mg_stream_t stream);
+
+/* Copy the last step's loss to the host; synchronises `stream`. */
+mg_status mg_loss(mg_plan* plan, float* host_loss, mg_stream_t stream);
+
+/* Device address of the last step's loss (one fp32), valid until destroy. */
+const float* mg_loss_device_ptr(const mg_plan* plan);
+
+/* Re-derive the bf16 weight copy from params (after the caller changed them,
+ * e.g. a checkpoint restore).  A no-op in strict mode. */
+mg_status mg_refresh_params(mg_plan* plan, const float* params, mg_stream_t stream);
+
+/* Human-readable schedule: one line per kernel with its shapes and the
+ * workspace offsets (the analogue of the pages' plan dump).  Writes at most
+ * cap bytes including the terminating NUL; returns the full length. */
+size_t mg_plan_dump(const mg_plan* plan, char* buf, size_t cap);
+
+/* Message of the last failure; NULL plan gives the process-wide message. */
+const char* mg_last_error(const mg_plan* plan);
+
+/* Scan n floats (device) for NaN/Inf; synchronises stream.  Returns
+ * MG_ERR_NONFINITE and the first bad index in *first_bad (may be NULL). */
+mg_status mg_debug_check_finite(mg_plan* plan, const float* data, size_t n, long long* first_bad,
+                                mg_stream_t stream);
+
+/* Kernels launched by the last mg_train_step / mg_forward call. */
+int mg_last_launch_count(const mg_plan* plan);
+
+/* ---- per-kernel timing (CUDA events around each launch) ----------------
+ * mg_profile_begin(plan, max_calls): from now on, each mg_train_step records
+ * a start/stop event pair around every kernel, for up to max_calls calls.
+ * mg_profile_end: synchronises, sums the elapsed time per schedule entry and
+ * stops recording.  mg_profile_entry reads entry i (a kernel of the step):
+ * its name, launches recorded, total milliseconds, and the algorithmic flops
+ * and DRAM bytes of one launch. */
+mg_status mg_profile_begin(mg_plan* plan, int max_calls);
+mg_status mg_profile_end(mg_plan* plan);
+int mg_profile_entries(const mg_plan* plan);
+mg_status mg_profile_entry(const mg_plan* plan, int i, char* name, size_t name_cap,
+                           int* launches, double* total_ms, double* flops, double* bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MG_H */

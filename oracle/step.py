@@ -26,11 +26,19 @@ where the pages are silent:
 * SGD: p -= lr g.  Adam (t = step, from 1): bias-corrected moments, eps added
   after the square root, no weight decay.
 
-Precision: float64 arithmetic throughout.  In the bf16 mode the inputs the
-fast path consumes in bf16 -- x, the weight matrices and the MSE target -- are
-rounded to bf16 (round to nearest even) first; everything else stays float64.
-Parameters and Adam moments are stored back as float32 after each update (the
-workloads keep fp32 master weights).
+Precision: float64 arithmetic throughout, with the storage types of the typed
+static graph.  Three modes:
+
+* "exact": every value kept in float64 (used by the finite-difference pins);
+* "strict": every graph value -- each layer's output and the gradient with
+  respect to each value -- is stored as float32 (strict f32);
+* "bf16": x, the weight matrices, the MSE target and every graph value and
+  value gradient are stored as bf16 (round to nearest even); the workloads'
+  "bf16 activations/weights, fp32 master weights and Adam moments".
+
+Arithmetic inside an op is float64 on the stored operands, rounded once to the
+value type.  Parameter gradients are float64; parameters and Adam moments are
+stored back as float32 after each update (fp32 master weights).
 
 Parity status: every function here is pinned by the CPU tests (finite
 differences, closed forms, brute force on tiny graphs, invariants, and PyTorch
@@ -57,6 +65,15 @@ def bf16_round(a) -> np.ndarray:
     lsb = (u >> np.uint64(16)) & np.uint64(1)
     r = ((u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)).astype(np.uint32)
     return r.view(np.float32).astype(np.float64)
+
+
+def store(a, precision):
+    """Round a value to the storage type of the graph's values."""
+    if precision == "bf16":
+        return bf16_round(a)
+    if precision == "strict":
+        return np.asarray(a, np.float64).astype(np.float32).astype(np.float64)
+    return np.asarray(a, np.float64)
 
 
 # --------------------------------------------------------------------------
@@ -177,11 +194,12 @@ def _param_slots(layers):
     return slots, i
 
 
-def forward(layers, params, x, precision="strict"):
-    """Returns (output [rows, d_out] float64, tape for backward)."""
+def forward(layers, params, x, precision="exact"):
+    """Returns (output [rows, d_out] float64, tape for backward).  Each layer's
+    output is a graph value, stored in the precision's value type."""
     slots, _ = _param_slots(layers)
     bf16 = precision == "bf16"
-    h = bf16_round(x) if bf16 else np.asarray(x, dtype=np.float64)
+    h = store(x, precision)
     tape, skips = [], []
     for l, sl in zip(layers, slots):
         op = l["op"]
@@ -207,6 +225,7 @@ def forward(layers, params, x, precision="strict"):
         elif op == "residual_begin":
             skips.append(h)
             tape.append({})
+            continue                       # no new value
         elif op == "residual_end":
             h = skips.pop() + h
             tape.append({})
@@ -216,13 +235,15 @@ def forward(layers, params, x, precision="strict"):
             h = o
         else:
             raise ValueError(op)
+        h = store(h, precision)
     if skips:
         raise ValueError("unbalanced residual_begin")
     return h, tape
 
 
-def loss_and_grad(kind, out, labels, precision="strict"):
-    """Loss (float) and dLoss/dout for the output of the last layer."""
+def loss_and_grad(kind, out, labels, precision="exact"):
+    """Loss (float) and dLoss/dout (in float64; backward stores it) for the
+    output of the last layer."""
     rows = out.shape[0]
     if kind == "ce_dense":
         y = np.asarray(labels, dtype=np.float64)
@@ -246,13 +267,17 @@ def loss_and_grad(kind, out, labels, precision="strict"):
     raise ValueError(kind)
 
 
-def backward(layers, params, tape, dout):
-    """Gradients of every parameter (float64), in declaration order."""
+def backward(layers, params, tape, dout, precision="exact"):
+    """Gradients of every parameter (float64), in declaration order, and the
+    gradient with respect to x.  The gradient with respect to each graph value
+    is stored in the value type once all its contributions are summed (a
+    residual's skip source receives two)."""
     slots, n = _param_slots(layers)
     grads = [None] * n
-    dh = dout
+    dh = store(dout, precision)
     skip_grads = []
-    for l, sl, t in zip(reversed(layers), reversed(slots), reversed(tape)):
+    rev = list(zip(layers, slots, tape))[::-1]
+    for k, (l, sl, t) in enumerate(rev):
         op = l["op"]
         if op == "linear":
             grads[sl[0]] = t["x"].T @ dh
@@ -270,12 +295,18 @@ def backward(layers, params, tape, dout):
             dh = r * (gy - x * r * r * (gy * x).mean(axis=1, keepdims=True))
         elif op == "residual_end":
             skip_grads.append(dh)
+            continue                       # the same value gradient flows to both
         elif op == "residual_begin":
             dh = dh + skip_grads.pop()
         elif op == "causal_attention":
             dh = attention_bwd(l, t["qkv"], t["p"], dh)
         else:
             raise ValueError(op)
+        # the value whose gradient dh now is: complete unless a residual_begin
+        # (which adds the skip's share) comes next in the reverse walk
+        if k + 1 < len(rev) and rev[k + 1][0]["op"] == "residual_begin":
+            continue
+        dh = store(dh, precision)
     return grads, dh
 
 
@@ -308,7 +339,7 @@ def train_step(layers, params, x, labels, loss_kind, precision, optimizer, lr, s
     params / moments."""
     out, tape = forward(layers, params, x, precision)
     loss, dout = loss_and_grad(loss_kind, out, labels, precision)
-    grads, _ = backward(layers, params, tape, dout)
+    grads, _ = backward(layers, params, tape, dout, precision)
     new_p, new_m, new_v = [], [], []
     for i, (p, g) in enumerate(zip(params, grads)):
         if optimizer == "sgd":

@@ -1,0 +1,86 @@
+// Internal (host-side) launchers of the training-step kernels.  Not part of
+// the C ABI; the plan in plan.cu calls these.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mg {
+
+enum DType { DT_F32 = 0, DT_BF16 = 1 };
+enum Act { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
+
+inline size_t dtype_size(DType t) { return t == DT_F32 ? 4 : 2; }
+
+// C[M,N] = A[M,K] * B[K,N] with fp32 accumulation and a fused epilogue:
+//   v = acc (+ bias[n]);  out_z = v;  v = act(v);  v *= act'(saved);  v += resid;  out = v
+// A(m,k) = a_mn ? A[k*lda + m] : A[m*lda + k]       (M-major or K-major storage)
+// B(k,n) = b_k  ? B[n*ldb + k] : B[k*ldb + n]       (K-major or N-major storage)
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr; long long lda = 0; int a_mn = 0;
+  const void* B = nullptr; long long ldb = 0; int b_k = 0;
+  DType in_type = DT_F32;
+  const float* bias = nullptr;
+  int act = 0;
+  void* out_z = nullptr; long long ldz = 0;
+  const void* saved = nullptr; long long lds = 0; int dact = 0;
+  const void* resid = nullptr; long long ldr = 0;
+  DType aux_type = DT_F32;   // dtype of out_z, saved, resid
+  void* out = nullptr; long long ldo = 0;
+  DType out_type = DT_F32;
+};
+
+cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
+
+// ---- loss ------------------------------------------------------------------
+// Softmax cross-entropy over rows of logits[B, C] (stride ld).  label_kind 0:
+// dense fp32 labels [B, C]; 1: int32 class ids [B].  Writes dlogits (same
+// dtype and layout as logits) = (p * sum(y) - y) / B, and row_loss[B] =
+// -sum_c y_c log p_c.  Then loss = sum(row_loss) / B.
+cudaError_t ce_loss(DType t, const void* logits, int B, int C, long long ld, int label_kind,
+                    const void* labels, void* dlogits, float* row_loss, float* loss,
+                    cudaStream_t s);
+// Mean squared error over n elements: dout = 2 (o - t) / n; loss = mean((o - t)^2).
+cudaError_t mse_loss(DType t, const void* o, const void* target, size_t n, void* dout,
+                     float* partials, int n_partials, float* loss, cudaStream_t s);
+
+// ---- reductions / norms ----------------------------------------------------
+// out[n] = sum over rows of src[r, n]  (fp32 result), deterministic two passes.
+cudaError_t colsum(DType t, const void* src, int rows, int cols, long long ld, float* partials,
+                   int row_chunks, float* out, cudaStream_t s);
+cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, float* rstd, int rows,
+                        int d, float eps, cudaStream_t s);
+// dx = r (g - x r^2 mean(g x)) + dadd, g = dy * gamma;  dgamma partial sums of dy * x * r.
+cudaError_t rmsnorm_bwd(DType t, const void* dy, const void* x, const float* rstd,
+                        const float* gamma, const void* dadd, void* dx, float* dgamma_partials,
+                        int row_chunks, float* dgamma, int rows, int d, cudaStream_t s);
+
+// ---- attention (bf16 storage, fp32 softmax) ----------------------------------
+// qkv [nb*S, 3*H*Dh], o [nb*S, H*Dh], lse [nb, H, S].
+cudaError_t attn_fwd(const void* qkv, void* o, float* lse, int nb, int S, int H, int Dh,
+                     cudaStream_t s);
+cudaError_t attn_bwd(const void* qkv, const void* o, const void* dout, const float* lse,
+                     float* dsum, void* dqkv, int nb, int S, int H, int Dh, cudaStream_t s);
+int attn_bwd_launches();
+
+// ---- optimizer (multi-tensor over chunk tables) -----------------------------
+struct Chunk {  // a run of one tensor's elements in the flat buffers
+  long long start;
+  int len;
+  int shadow;   // 1: write the bf16 copy of the updated value
+};
+cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
+                        float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
+                        float beta1, float beta2, float eps, cudaStream_t s);
+cudaError_t sgd_update(const Chunk* chunks, int n_chunks, float* p, const float* g, void* shadow,
+                       float lr, cudaStream_t s);
+cudaError_t cast_shadow(const Chunk* chunks, int n_chunks, const float* p, void* shadow,
+                        cudaStream_t s);
+
+// ---- misc --------------------------------------------------------------------
+cudaError_t cast_to_f32(DType t, const void* src, float* dst, size_t n, cudaStream_t s);
+cudaError_t find_nonfinite(const float* data, size_t n, unsigned long long* first_bad,
+                           cudaStream_t s);
+
+}  // namespace mg

@@ -1,0 +1,136 @@
+// Loss kernels: row softmax cross-entropy (+ its gradient) and mean squared
+// error (+ its gradient), the reduction archetype of the Meganeura README
+// (Example section: cross_entropy_loss(logits, labels) with a dense [B, C]
+// label tensor; "Why Meganeura" section: the reduction kernel archetype).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mg {
+namespace {
+
+// Deterministic sum of v[0..n) times scale, one block.
+__global__ void __launch_bounds__(1024) reduce_sum_kernel(const float* v, int n, float scale,
+                                                          float* out) {
+  __shared__ float red[32];
+  float s = 0.0f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s += v[i];
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) *out = s * scale;
+}
+
+// One block per row.  Pass 1: running (max, sum of exp) per thread, merged
+// across the block; pass 2: gradient.  Labels: dense fp32 [B, C] or int32 ids.
+template <typename T, bool DENSE>
+__global__ void __launch_bounds__(256) ce_kernel(const T* logits, int C, long long ld,
+                                                 const void* labels, T* dlogits,
+                                                 float* row_loss, float inv_b) {
+  __shared__ float red[32];
+  __shared__ float sh_m, sh_s;
+  const int r = blockIdx.x;
+  const T* z = logits + (size_t)r * ld;
+  T* dz = dlogits + (size_t)r * ld;
+
+  float m = -INFINITY, s = 0.0f;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float x = ld_elem(z, c);
+    if (x > m) {
+      s = s * expf(m - x) + 1.0f;
+      m = x;
+    } else {
+      s += expf(x - m);
+    }
+  }
+  // merge (m, s) across the block
+  float bm = block_max(m, red);
+  float sc = (m == -INFINITY) ? 0.0f : s * expf(m - bm);
+  float bs = block_sum(sc, red);
+  if (threadIdx.x == 0) {
+    sh_m = bm;
+    sh_s = bs;
+  }
+  __syncthreads();
+  const float lse = sh_m + logf(sh_s);
+
+  float ysum = 1.0f, yz = 0.0f;
+  if (DENSE) {
+    const float* y = static_cast<const float*>(labels) + (size_t)r * C;
+    float a = 0.0f, b = 0.0f;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      float yc = y[c];
+      a += yc;
+      b += yc * ld_elem(z, c);
+    }
+    ysum = block_sum(a, red);
+    yz = block_sum(b, red);
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      float p = expf(ld_elem(z, c) - lse);
+      st_elem(dz, c, (p * ysum - y[c]) * inv_b);
+    }
+    if (threadIdx.x == 0) row_loss[r] = lse * ysum - yz;
+  } else {
+    const int t = static_cast<const int*>(labels)[r];
+    const bool ok = t >= 0 && t < C;      // an id outside [0, C) poisons the loss (NaN)
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      float p = expf(ld_elem(z, c) - lse);
+      st_elem(dz, c, (p - (c == t ? 1.0f : 0.0f)) * inv_b);
+    }
+    if (threadIdx.x == 0) row_loss[r] = ok ? lse - ld_elem(z, t) : __int_as_float(0x7fc00000);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) mse_kernel(const T* o, const T* t, size_t n, T* dout,
+                                                  float* partials, float two_over_n) {
+  __shared__ float red[32];
+  float acc = 0.0f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float d = ld_elem(o, i) - ld_elem(t, i);
+    acc += d * d;
+    st_elem(dout, i, d * two_over_n);
+  }
+  acc = block_sum(acc, red);
+  if (threadIdx.x == 0) partials[blockIdx.x] = acc;
+}
+
+}  // namespace
+
+cudaError_t ce_loss(DType t, const void* logits, int B, int C, long long ld, int label_kind,
+                    const void* labels, void* dlogits, float* row_loss, float* loss,
+                    cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  float inv_b = 1.0f / (float)B;
+  if (t == DT_F32) {
+    if (label_kind == 0)
+      ce_kernel<float, true><<<B, 256, 0, s>>>((const float*)logits, C, ld, labels,
+                                               (float*)dlogits, row_loss, inv_b);
+    else
+      ce_kernel<float, false><<<B, 256, 0, s>>>((const float*)logits, C, ld, labels,
+                                                (float*)dlogits, row_loss, inv_b);
+  } else {
+    if (label_kind == 0)
+      ce_kernel<bf16, true><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels,
+                                              (bf16*)dlogits, row_loss, inv_b);
+    else
+      ce_kernel<bf16, false><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels,
+                                               (bf16*)dlogits, row_loss, inv_b);
+  }
+  reduce_sum_kernel<<<1, 1024, 0, s>>>(row_loss, B, inv_b, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t mse_loss(DType t, const void* o, const void* target, size_t n, void* dout,
+                     float* partials, int n_partials, float* loss, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  float two_over_n = (float)(2.0 / (double)n);
+  if (t == DT_F32)
+    mse_kernel<float><<<n_partials, 256, 0, s>>>((const float*)o, (const float*)target, n,
+                                                 (float*)dout, partials, two_over_n);
+  else
+    mse_kernel<bf16><<<n_partials, 256, 0, s>>>((const bf16*)o, (const bf16*)target, n,
+                                                (bf16*)dout, partials, two_over_n);
+  reduce_sum_kernel<<<1, 1024, 0, s>>>(partials, n_partials, (float)(1.0 / (double)n), loss);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

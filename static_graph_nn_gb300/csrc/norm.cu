@@ -1,0 +1,154 @@
+// RMSNorm forward/backward and column sums (bias and gamma gradients): the
+// reduction archetype of the Meganeura README ("Why Meganeura" section).
+//
+// RMSNorm: r = 1/sqrt(mean(x^2) + eps), y = x r gamma.  Backward with g = dy
+// gamma: dx = r (g - x r^2 mean(g x)), dgamma = sum_rows dy x r.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mg {
+namespace {
+
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_MAX_PER_THREAD = 16;   // d <= 4096
+
+template <typename T>
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_kernel(const T* x, const float* gamma,
+                                                                    T* y, float* rstd, int rows,
+                                                                    int d, float eps) {
+  __shared__ float red[32];
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* xr = x + (size_t)r * d;
+    float v[NORM_MAX_PER_THREAD];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) {
+      int c = threadIdx.x + i * NORM_THREADS;
+      v[i] = c < d ? ld_elem(xr, c) : 0.0f;
+      ss += v[i] * v[i];
+    }
+    ss = block_sum(ss, red);
+    float rs = 1.0f / sqrtf(ss / (float)d + eps);
+    if (threadIdx.x == 0) rstd[r] = rs;
+    T* yr = y + (size_t)r * d;
+#pragma unroll
+    for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) {
+      int c = threadIdx.x + i * NORM_THREADS;
+      if (c < d) st_elem(yr, c, v[i] * rs * gamma[c]);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_kernel(
+    const T* dy, const T* x, const float* rstd, const float* gamma, const T* dadd, T* dx,
+    float* dgamma_partials, int rows, int d) {
+  __shared__ float red[32];
+  float dg[NORM_MAX_PER_THREAD];
+#pragma unroll
+  for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) dg[i] = 0.0f;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const T* dyr = dy + (size_t)r * d;
+    const T* xr = x + (size_t)r * d;
+    const float rs = rstd[r];
+    float xv[NORM_MAX_PER_THREAD], gv[NORM_MAX_PER_THREAD];
+    float gx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) {
+      int c = threadIdx.x + i * NORM_THREADS;
+      float dyc = c < d ? ld_elem(dyr, c) : 0.0f;
+      xv[i] = c < d ? ld_elem(xr, c) : 0.0f;
+      gv[i] = c < d ? dyc * gamma[c] : 0.0f;
+      dg[i] += dyc * xv[i] * rs;
+      gx += gv[i] * xv[i];
+    }
+    if (dx) {
+      gx = block_sum(gx, red) / (float)d;
+      const float k = rs * rs * gx;
+      T* dxr = dx + (size_t)r * d;
+      const T* ar = dadd ? dadd + (size_t)r * d : nullptr;
+#pragma unroll
+      for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) {
+        int c = threadIdx.x + i * NORM_THREADS;
+        if (c < d) {
+          float val = rs * (gv[i] - xv[i] * k);
+          if (ar) val += ld_elem(ar, c);
+          st_elem(dxr, c, val);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NORM_MAX_PER_THREAD; ++i) {
+    int c = threadIdx.x + i * NORM_THREADS;
+    if (c < d) dgamma_partials[(size_t)blockIdx.x * d + c] = dg[i];
+  }
+}
+
+// partials[chunk, c] = sum of src[r, c] over the rows of this chunk.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_pass1(const T* src, int rows, int cols, long long ld,
+                                                    float* partials) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  int chunks = gridDim.y;
+  int per = (rows + chunks - 1) / chunks;
+  int r0 = blockIdx.y * per, r1 = min(rows, r0 + per);
+  float s = 0.0f;
+  for (int r = r0; r < r1; ++r) s += ld_elem(src, (size_t)r * ld + c);
+  partials[(size_t)blockIdx.y * cols + c] = s;
+}
+
+__global__ void __launch_bounds__(256) colsum_pass2(const float* partials, int chunks, int cols,
+                                                    float* out) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.0f;
+  for (int k = 0; k < chunks; ++k) s += partials[(size_t)k * cols + c];
+  out[c] = s;
+}
+
+}  // namespace
+
+cudaError_t colsum(DType t, const void* src, int rows, int cols, long long ld, float* partials,
+                   int row_chunks, float* out, cudaStream_t s) {
+  if (cols <= 0) return cudaSuccess;
+  dim3 g1((cols + 255) / 256, row_chunks);
+  if (t == DT_F32)
+    colsum_pass1<float><<<g1, 256, 0, s>>>((const float*)src, rows, cols, ld, partials);
+  else
+    colsum_pass1<bf16><<<g1, 256, 0, s>>>((const bf16*)src, rows, cols, ld, partials);
+  colsum_pass2<<<(cols + 255) / 256, 256, 0, s>>>(partials, row_chunks, cols, out);
+  return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, float* rstd, int rows,
+                        int d, float eps, cudaStream_t s) {
+  if (d > NORM_THREADS * NORM_MAX_PER_THREAD) return cudaErrorInvalidValue;
+  int grid = rows < 152 * 16 ? rows : 152 * 16;
+  if (t == DT_F32)
+    rmsnorm_fwd_kernel<float><<<grid, NORM_THREADS, 0, s>>>((const float*)x, gamma, (float*)y,
+                                                            rstd, rows, d, eps);
+  else
+    rmsnorm_fwd_kernel<bf16><<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd,
+                                                           rows, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t rmsnorm_bwd(DType t, const void* dy, const void* x, const float* rstd,
+                        const float* gamma, const void* dadd, void* dx, float* dgamma_partials,
+                        int row_chunks, float* dgamma, int rows, int d, cudaStream_t s) {
+  if (d > NORM_THREADS * NORM_MAX_PER_THREAD) return cudaErrorInvalidValue;
+  if (t == DT_F32)
+    rmsnorm_bwd_kernel<float><<<row_chunks, NORM_THREADS, 0, s>>>(
+        (const float*)dy, (const float*)x, rstd, gamma, (const float*)dadd, (float*)dx,
+        dgamma_partials, rows, d);
+  else
+    rmsnorm_bwd_kernel<bf16><<<row_chunks, NORM_THREADS, 0, s>>>(
+        (const bf16*)dy, (const bf16*)x, rstd, gamma, (const bf16*)dadd, (bf16*)dx,
+        dgamma_partials, rows, d);
+  colsum_pass2<<<(d + 255) / 256, 256, 0, s>>>(dgamma_partials, row_chunks, d, dgamma);
+  return cudaGetLastError();
+}
+
+}  // namespace mg

@@ -1,0 +1,902 @@
+// The step plan: descriptor validation, parameter layout, workspace, and the
+// fixed kernel schedule of one training step (forward, loss, backward,
+// optimizer), behind the C ABI declared in include/mg.h.
+//
+// This is the GPU-side counterpart of the Meganeura pages' build_session
+// (README Example section: autodiff + compile + GPU init happen once) and of
+// its memory planner (abstract): here every value and every gradient gets its
+// own region of one workspace allocated at creation, and the backward pass is
+// derived by hand per fused node:
+//   Linear (+ bias, + ReLU/GELU, + residual add) -> one GEMM with a fused epilogue
+//   RMSNorm, causal attention                    -> their own kernels
+//   cross-entropy / MSE                           -> a loss+gradient kernel
+//   SGD / Adam                                    -> one multi-tensor kernel
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/mg.h"
+#include "kernels.h"
+
+using namespace mg;
+
+namespace {
+
+std::mutex g_err_mu;
+std::string g_err = "";
+
+constexpr size_t kAlignElems = 64;      // parameter offsets (256 B in fp32)
+constexpr size_t kWsAlign = 1024;       // workspace region alignment
+constexpr int kChunk = 16384;           // optimizer chunk (elements)
+constexpr int kRowChunks = 64;          // column-sum partial rows
+constexpr int kMsePartials = 1024;
+
+enum NodeKind { NK_LINEAR, NK_RMSNORM, NK_ATTN };
+
+struct Value {
+  int width = 0;
+  size_t off = 0;        // workspace offset (value 0 = caller's x)
+  size_t goff = 0;       // workspace offset of its gradient
+  bool has_grad = false;
+  bool need_grad = false;
+  int producer = -1;     // node index
+  int producer_act = 0;  // activation fused into the producing Linear
+  int z_value = -1;      // saved pre-activation (GELU) of the producer
+  int pending_add = -1;  // value whose gradient also flows into this one (skip)
+  int consumers = 0;
+};
+
+struct Node {
+  NodeKind kind;
+  int layer = 0;
+  int in = -1, out = -1;
+  // linear
+  int d_in = 0, d_out = 0, has_bias = 0, act = 0, skip = -1, z = -1;
+  size_t w_off = 0, b_off = 0;
+  // rmsnorm
+  int d = 0;
+  float eps = 0.f;
+  size_t g_off = 0, rstd_off = 0;
+  // attention
+  int nh = 0, dh = 0, S = 0;
+  size_t lse_off = 0, dsum_off = 0;
+};
+
+struct Site {
+  std::string name;
+  double flops = 0, bytes = 0;
+  int kernels = 1;
+  int launches = 0;
+  double total_ms = 0;
+};
+
+}  // namespace
+
+struct mg_plan {
+  int device = 0;
+  int batch = 0;
+  int loss = 0, precision = 0, optimizer = 0;
+  float beta1 = 0.9f, beta2 = 0.999f, adam_eps = 1e-8f;
+  DType dt = DT_F32;
+  std::vector<mg_layer> layers;
+  std::vector<Value> values;
+  std::vector<Node> nodes;
+  int final_value = 0;
+  // parameters
+  std::vector<size_t> p_off;
+  std::vector<int> p_rows, p_cols;
+  std::vector<int> p_is_weight;
+  size_t n_params = 0;
+  // workspace
+  size_t ws_bytes = 0;
+  char* ws = nullptr;
+  size_t shadow_off = 0, chunks_off = 0, loss_off = 0, rowloss_off = 0, partial_off = 0,
+         flag_off = 0;
+  int n_chunks = 0;
+  const float* last_params = nullptr;
+  // schedule bookkeeping
+  std::vector<Site> sites;
+  int last_launches = 0;
+  bool profiling = false;
+  int prof_max = 0, prof_calls = 0;
+  std::vector<cudaEvent_t> events;
+  std::string err;
+  std::string dump;
+};
+
+namespace {
+
+mg_status fail(mg_plan* p, mg_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (p) p->err = buf;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  g_err = buf;
+  return st;
+}
+
+mg_status cuda_fail(mg_plan* p, cudaError_t e, const char* what) {
+  return fail(p, MG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Bump {
+  size_t top = 0;
+  size_t take(size_t bytes) {
+    size_t o = round_up(top, kWsAlign);
+    top = o + round_up(bytes, 16);
+    return o;
+  }
+};
+
+// ---- execution context ---------------------------------------------------
+struct Exec {
+  mg_plan* p;
+  cudaStream_t s;
+  bool dry;          // only register sites
+  bool profile;      // record events around each site
+  int cursor = 0;
+  int launches = 0;
+  cudaError_t err = cudaSuccess;
+};
+
+template <class F>
+void site(Exec& e, const std::string& name, double flops, double bytes, int kernels, F&& f) {
+  mg_plan* p = e.p;
+  int id = e.cursor++;
+  if (e.dry) {
+    Site st;
+    st.name = name;
+    st.flops = flops;
+    st.bytes = bytes;
+    st.kernels = kernels;
+    p->sites.push_back(st);
+    return;
+  }
+  if (e.err != cudaSuccess) return;
+  const int ns = (int)p->sites.size();
+  const bool rec = e.profile && p->profiling && p->prof_calls < p->prof_max && id < ns;
+  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2], e.s);
+  cudaError_t r = f();
+  if (r != cudaSuccess) e.err = r;
+  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2 + 1], e.s);
+  e.launches += kernels;
+}
+
+template <class T>
+T* wsp(mg_plan* p, size_t off) {
+  return reinterpret_cast<T*>(p->ws + off);
+}
+
+const void* val_ptr(mg_plan* p, int v, const void* x) {
+  return v == 0 ? x : (const void*)(p->ws + p->values[v].off);
+}
+
+void* grad_ptr(mg_plan* p, int v) { return p->ws + p->values[v].goff; }
+
+double gemm_bytes(const GemmArgs& g) {
+  double in = (double)dtype_size(g.in_type), aux = (double)dtype_size(g.aux_type);
+  double b = ((double)g.M * g.K + (double)g.K * g.N) * in + (double)g.M * g.N * dtype_size(g.out_type);
+  if (g.bias) b += 4.0 * g.N;
+  if (g.out_z) b += aux * g.M * g.N;
+  if (g.dact) b += aux * g.M * g.N;
+  if (g.resid) b += aux * g.M * g.N;
+  return b;
+}
+
+cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) { return gemm_simt(g, s); }
+
+std::string gemm_name(const char* what, int layer, const GemmArgs& g) {
+  char b[160];
+  snprintf(b, sizeof b, "%s[l%d] %dx%dx%d %s", what, layer, g.M, g.N, g.K,
+           g.in_type == DT_BF16 ? "bf16" : "f32-ffma");
+  return b;
+}
+
+// ---- the schedule ----------------------------------------------------------
+void forward_pass(Exec& e, const float* params, const void* x) {
+  mg_plan* p = e.p;
+  const DType dt = p->dt;
+  const void* wbase = dt == DT_BF16 ? (const void*)(p->ws + p->shadow_off) : (const void*)params;
+  for (size_t ni = 0; ni < p->nodes.size(); ++ni) {
+    const Node& n = p->nodes[ni];
+    if (n.kind == NK_LINEAR) {
+      GemmArgs g;
+      g.M = p->batch; g.N = n.d_out; g.K = n.d_in;
+      g.A = val_ptr(p, n.in, x); g.lda = n.d_in; g.a_mn = 0;
+      g.B = (const char*)wbase + n.w_off * dtype_size(dt); g.ldb = n.d_out; g.b_k = 0;
+      g.in_type = dt;
+      g.bias = n.has_bias ? params + n.b_off : nullptr;
+      g.act = n.act;
+      if (n.z >= 0) { g.out_z = p->ws + p->values[n.z].off; g.ldz = n.d_out; }
+      if (n.skip >= 0) { g.resid = val_ptr(p, n.skip, x); g.ldr = n.d_out; }
+      g.aux_type = dt;
+      g.out = p->ws + p->values[n.out].off; g.ldo = n.d_out; g.out_type = dt;
+      site(e, gemm_name("fwd", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+           [&] { return run_gemm(g, e.s); });
+    } else if (n.kind == NK_RMSNORM) {
+      double bytes = 2.0 * dtype_size(dt) * p->batch * n.d + 4.0 * n.d + 4.0 * p->batch;
+      char nm[96];
+      snprintf(nm, sizeof nm, "rmsnorm_fwd[l%d] %dx%d", n.layer, p->batch, n.d);
+      site(e, nm, 0, bytes, 1, [&] {
+        return rmsnorm_fwd(dt, val_ptr(p, n.in, x), params + n.g_off, p->ws + p->values[n.out].off,
+                           wsp<float>(p, n.rstd_off), p->batch, n.d, n.eps, e.s);
+      });
+    } else {
+      int nb = p->batch / n.S;
+      double pairs = (double)n.S * (n.S + 1) / 2.0;
+      double flops = 4.0 * nb * n.nh * pairs * n.dh;
+      double bytes = 2.0 * p->batch * 4.0 * n.nh * n.dh + 4.0 * nb * n.nh * n.S;
+      char nm[96];
+      snprintf(nm, sizeof nm, "attn_fwd[l%d] b%d s%d h%d d%d", n.layer, nb, n.S, n.nh, n.dh);
+      site(e, nm, flops, bytes, 1, [&] {
+        return attn_fwd(val_ptr(p, n.in, x), p->ws + p->values[n.out].off,
+                        wsp<float>(p, n.lse_off), nb, n.S, n.nh, n.dh, e.s);
+      });
+    }
+  }
+}
+
+void loss_pass(Exec& e, const void* labels) {
+  mg_plan* p = e.p;
+  const DType dt = p->dt;
+  const Value& f = p->values[p->final_value];
+  const int C = f.width, B = p->batch;
+  const void* logits = p->ws + f.off;
+  void* dlogits = p->ws + f.goff;
+  if (p->loss == MG_LOSS_MSE) {
+    size_t n = (size_t)B * C;
+    site(e, "mse_loss", 0, 3.0 * dtype_size(dt) * n, 2, [&] {
+      return mse_loss(dt, logits, labels, n, dlogits, wsp<float>(p, p->partial_off), kMsePartials,
+                      wsp<float>(p, p->loss_off), e.s);
+    });
+  } else {
+    int kind = p->loss == MG_LOSS_CE_DENSE ? 0 : 1;
+    double bytes = 2.0 * dtype_size(dt) * B * C + (kind == 0 ? 4.0 * B * C : 4.0 * B);
+    char nm[96];
+    snprintf(nm, sizeof nm, "softmax_ce_%s %dx%d", kind == 0 ? "dense" : "index", B, C);
+    site(e, nm, 0, bytes, 2, [&] {
+      return ce_loss(dt, logits, B, C, C, kind, labels, dlogits, wsp<float>(p, p->rowloss_off),
+                     wsp<float>(p, p->loss_off), e.s);
+    });
+  }
+}
+
+void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
+  mg_plan* p = e.p;
+  const DType dt = p->dt;
+  const void* wbase = dt == DT_BF16 ? (const void*)(p->ws + p->shadow_off) : (const void*)params;
+  for (int ni = (int)p->nodes.size() - 1; ni >= 0; --ni) {
+    const Node& n = p->nodes[ni];
+    if (!p->values[n.out].need_grad) continue;
+    const void* gy = grad_ptr(p, n.out);
+    const Value& vin = p->values[n.in];
+    const void* dadd = vin.pending_add >= 0 ? grad_ptr(p, vin.pending_add) : nullptr;
+    if (n.kind == NK_LINEAR) {
+      // dW = X^T dZ   (M = d_in, N = d_out, K = batch)
+      GemmArgs g;
+      g.M = n.d_in; g.N = n.d_out; g.K = p->batch;
+      g.A = val_ptr(p, n.in, x); g.lda = n.d_in; g.a_mn = 1;
+      g.B = gy; g.ldb = n.d_out; g.b_k = 0;
+      g.in_type = dt; g.aux_type = dt;
+      g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
+      site(e, gemm_name("dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+           [&] { return run_gemm(g, e.s); });
+      if (n.has_bias) {
+        char nm[96];
+        snprintf(nm, sizeof nm, "db_colsum[l%d] %dx%d", n.layer, p->batch, n.d_out);
+        site(e, nm, 0, (double)dtype_size(dt) * p->batch * n.d_out + 4.0 * n.d_out, 2, [&] {
+          return colsum(dt, gy, p->batch, n.d_out, n.d_out, wsp<float>(p, p->partial_off),
+                        kRowChunks, grads + n.b_off, e.s);
+        });
+      }
+      if (vin.need_grad) {
+        // dX = dZ W^T, times act'(saved) of the producer of X, plus the skip gradient
+        GemmArgs h;
+        h.M = p->batch; h.N = n.d_in; h.K = n.d_out;
+        h.A = gy; h.lda = n.d_out; h.a_mn = 0;
+        h.B = (const char*)wbase + n.w_off * dtype_size(dt); h.ldb = n.d_out; h.b_k = 1;
+        h.in_type = dt; h.aux_type = dt;
+        if (vin.producer_act) {
+          h.dact = vin.producer_act;
+          int sv = vin.producer_act == ACT_GELU ? vin.z_value : n.in;
+          h.saved = p->ws + p->values[sv].off;
+          h.lds = n.d_in;
+        }
+        if (dadd) { h.resid = dadd; h.ldr = n.d_in; }
+        h.out = grad_ptr(p, n.in); h.ldo = n.d_in; h.out_type = dt;
+        site(e, gemm_name("dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
+             [&] { return run_gemm(h, e.s); });
+      }
+    } else if (n.kind == NK_RMSNORM) {
+      void* dx = vin.need_grad ? grad_ptr(p, n.in) : nullptr;
+      double bytes = (double)dtype_size(dt) * p->batch * n.d * (dx ? (dadd ? 4 : 3) : 2);
+      char nm[96];
+      snprintf(nm, sizeof nm, "rmsnorm_bwd[l%d] %dx%d", n.layer, p->batch, n.d);
+      site(e, nm, 0, bytes, 2, [&] {
+        return rmsnorm_bwd(dt, gy, val_ptr(p, n.in, x), wsp<float>(p, n.rstd_off),
+                           params + n.g_off, dx ? dadd : nullptr, dx,
+                           wsp<float>(p, p->partial_off), kRowChunks, grads + n.g_off,
+                           p->batch, n.d, e.s);
+      });
+    } else {
+      if (!vin.need_grad) continue;
+      int nb = p->batch / n.S;
+      double pairs = (double)n.S * (n.S + 1) / 2.0;
+      double flops = 10.0 * nb * n.nh * pairs * n.dh;
+      double bytes = 2.0 * p->batch * n.nh * n.dh * (3 + 2 + 3);
+      char nm[96];
+      snprintf(nm, sizeof nm, "attn_bwd[l%d] b%d s%d h%d d%d", n.layer, nb, n.S, n.nh, n.dh);
+      site(e, nm, flops, bytes, attn_bwd_launches(), [&] {
+        return attn_bwd(val_ptr(p, n.in, x), p->ws + p->values[n.out].off, gy,
+                        wsp<float>(p, n.lse_off), wsp<float>(p, n.dsum_off), grad_ptr(p, n.in), nb,
+                        n.S, n.nh, n.dh, e.s);
+      });
+    }
+  }
+}
+
+void optimizer_pass(Exec& e, float* params, float* grads, float* m, float* v, float lr, int step) {
+  mg_plan* p = e.p;
+  const Chunk* chunks = wsp<Chunk>(p, p->chunks_off);
+  void* shadow = p->dt == DT_BF16 ? p->ws + p->shadow_off : nullptr;
+  double np = (double)p->n_params;
+  if (p->optimizer == MG_OPT_ADAM) {
+    double bc1 = 1.0 - std::pow((double)p->beta1, (double)step);
+    double bc2 = 1.0 - std::pow((double)p->beta2, (double)step);
+    float lr_bc1 = (float)(lr / bc1), inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    site(e, "adam_multi_tensor", 0, np * (28.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
+      return adam_update(chunks, p->n_chunks, params, grads, m, v, shadow, lr_bc1, inv_sqrt_bc2,
+                         p->beta1, p->beta2, p->adam_eps, e.s);
+    });
+  } else {
+    site(e, "sgd_multi_tensor", 0, np * (12.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
+      return sgd_update(chunks, p->n_chunks, params, grads, shadow, lr, e.s);
+    });
+  }
+}
+
+void train_schedule(Exec& e, float* params, float* grads, float* m, float* v, const void* x,
+                    const void* labels, float lr, int step) {
+  forward_pass(e, params, x);
+  loss_pass(e, labels);
+  backward_pass(e, params, grads, x);
+  optimizer_pass(e, params, grads, m, v, lr, step);
+}
+
+// ---- descriptor compile ------------------------------------------------------
+mg_status compile(mg_plan* p, const mg_graph_desc* d) {
+  if (d->batch <= 0) return fail(p, MG_ERR_SHAPE, "batch must be positive (got %d)", d->batch);
+  if (d->n_layers <= 0 || !d->layers) return fail(p, MG_ERR_INVALID_ARG, "graph has no layers");
+  if (d->loss < 0 || d->loss > 2) return fail(p, MG_ERR_INVALID_ARG, "bad loss kind %d", d->loss);
+  if (d->precision < 0 || d->precision > 1)
+    return fail(p, MG_ERR_INVALID_ARG, "bad precision %d", d->precision);
+  if (d->optimizer < 0 || d->optimizer > 1)
+    return fail(p, MG_ERR_INVALID_ARG, "bad optimizer %d", d->optimizer);
+  if (d->optimizer == MG_OPT_ADAM &&
+      !(d->beta1 >= 0 && d->beta1 < 1 && d->beta2 >= 0 && d->beta2 < 1 && d->adam_eps > 0))
+    return fail(p, MG_ERR_INVALID_ARG, "Adam needs 0 <= beta < 1 and eps > 0");
+  p->batch = d->batch;
+  p->loss = d->loss;
+  p->precision = d->precision;
+  p->optimizer = d->optimizer;
+  p->beta1 = d->beta1;
+  p->beta2 = d->beta2;
+  p->adam_eps = d->adam_eps;
+  p->dt = d->precision == MG_PREC_BF16 ? DT_BF16 : DT_F32;
+  p->layers.assign(d->layers, d->layers + d->n_layers);
+
+  // input width
+  int w0 = -1;
+  for (auto& l : p->layers) {
+    if (l.op == MG_OP_LINEAR) { w0 = l.d_in; break; }
+    if (l.op == MG_OP_RMSNORM) { w0 = l.d_in; break; }
+    if (l.op == MG_OP_CAUSAL_ATTENTION) { w0 = 3 * l.n_heads * l.head_dim; break; }
+  }
+  if (w0 <= 0) return fail(p, MG_ERR_SHAPE, "cannot infer the input width");
+  p->values.clear();
+  p->nodes.clear();
+  Value vx;
+  vx.width = w0;
+  p->values.push_back(vx);
+  int cur = 0;
+  std::vector<int> skips;
+  size_t poff = 0;
+  auto add_param = [&](int rows, int cols, int is_w) {
+    poff = round_up(poff, kAlignElems);
+    p->p_off.push_back(poff);
+    p->p_rows.push_back(rows);
+    p->p_cols.push_back(cols);
+    p->p_is_weight.push_back(is_w);
+    size_t o = poff;
+    poff += (size_t)rows * cols;
+    return o;
+  };
+  auto new_value = [&](int width, int producer) {
+    Value v;
+    v.width = width;
+    v.producer = producer;
+    p->values.push_back(v);
+    return (int)p->values.size() - 1;
+  };
+  const int nl = (int)p->layers.size();
+  for (int i = 0; i < nl; ++i) {
+    const mg_layer& l = p->layers[i];
+    Value& vc = p->values[cur];
+    switch (l.op) {
+      case MG_OP_LINEAR: {
+        if (l.d_in <= 0 || l.d_out <= 0) return fail(p, MG_ERR_SHAPE, "layer %d: bad Linear widths", i);
+        if (l.d_in != vc.width)
+          return fail(p, MG_ERR_SHAPE, "layer %d: Linear d_in %d != incoming width %d", i, l.d_in, vc.width);
+        Node n;
+        n.kind = NK_LINEAR;
+        n.layer = i;
+        n.in = cur;
+        n.d_in = l.d_in;
+        n.d_out = l.d_out;
+        n.has_bias = l.has_bias ? 1 : 0;
+        n.w_off = add_param(l.d_in, l.d_out, 1);
+        if (n.has_bias) n.b_off = add_param(1, l.d_out, 0);
+        if (i + 1 < nl && (p->layers[i + 1].op == MG_OP_RELU || p->layers[i + 1].op == MG_OP_GELU_TANH)) {
+          n.act = p->layers[i + 1].op == MG_OP_RELU ? ACT_RELU : ACT_GELU;
+          ++i;
+          if (i + 1 < nl && p->layers[i + 1].op == MG_OP_RESIDUAL_END)
+            return fail(p, MG_ERR_UNSUPPORTED, "layer %d: an activation directly before a residual end", i);
+        }
+        if (i + 1 < nl && p->layers[i + 1].op == MG_OP_RESIDUAL_END) {
+          if (skips.empty()) return fail(p, MG_ERR_INVALID_ARG, "layer %d: residual end without begin", i + 1);
+          n.skip = skips.back();
+          skips.pop_back();
+          if (p->values[n.skip].width != l.d_out)
+            return fail(p, MG_ERR_SHAPE, "layer %d: residual widths differ (%d vs %d)", i + 1,
+                        p->values[n.skip].width, l.d_out);
+          ++i;
+        }
+        int ni = (int)p->nodes.size();
+        if (n.act == ACT_GELU) n.z = new_value(l.d_out, ni);
+        n.out = new_value(l.d_out, ni);
+        p->values[n.out].producer_act = n.act;
+        p->values[n.out].z_value = n.z;
+        p->values[n.in].consumers++;
+        p->nodes.push_back(n);
+        cur = n.out;
+        break;
+      }
+      case MG_OP_RMSNORM: {
+        if (l.d_in != vc.width)
+          return fail(p, MG_ERR_SHAPE, "layer %d: RMSNorm width %d != incoming width %d", i, l.d_in, vc.width);
+        if (l.d_in > 4096) return fail(p, MG_ERR_UNSUPPORTED, "layer %d: RMSNorm width above 4096", i);
+        if (!(l.eps >= 0)) return fail(p, MG_ERR_INVALID_ARG, "layer %d: RMSNorm eps < 0", i);
+        if (vc.producer_act) return fail(p, MG_ERR_UNSUPPORTED, "layer %d: RMSNorm after an activation", i);
+        Node n;
+        n.kind = NK_RMSNORM;
+        n.layer = i;
+        n.in = cur;
+        n.d = l.d_in;
+        n.eps = l.eps;
+        n.g_off = add_param(1, l.d_in, 0);
+        int ni = (int)p->nodes.size();
+        n.out = new_value(l.d_in, ni);
+        p->values[n.in].consumers++;
+        p->nodes.push_back(n);
+        cur = n.out;
+        break;
+      }
+      case MG_OP_RESIDUAL_BEGIN:
+        if (vc.producer_act) return fail(p, MG_ERR_UNSUPPORTED, "layer %d: residual source is an activation output", i);
+        skips.push_back(cur);
+        break;
+      case MG_OP_RESIDUAL_END:
+        return fail(p, MG_ERR_UNSUPPORTED, "layer %d: residual end must directly follow a Linear", i);
+      case MG_OP_RELU:
+      case MG_OP_GELU_TANH:
+        return fail(p, MG_ERR_UNSUPPORTED, "layer %d: activation must directly follow a Linear", i);
+      case MG_OP_CAUSAL_ATTENTION: {
+        if (p->dt != DT_BF16) return fail(p, MG_ERR_UNSUPPORTED, "layer %d: attention needs bf16 precision", i);
+        if (l.n_heads <= 0 || l.head_dim != 64)
+          return fail(p, MG_ERR_UNSUPPORTED, "layer %d: attention supports head_dim 64 only", i);
+        if (l.seq_len <= 0 || l.seq_len % 64)
+          return fail(p, MG_ERR_UNSUPPORTED, "layer %d: seq_len must be a positive multiple of 64", i);
+        if (d->batch % l.seq_len) return fail(p, MG_ERR_SHAPE, "layer %d: batch not a multiple of seq_len", i);
+        if (vc.width != 3 * l.n_heads * l.head_dim)
+          return fail(p, MG_ERR_SHAPE, "layer %d: attention input width %d != 3*%d*%d", i, vc.width,
+                      l.n_heads, l.head_dim);
+        if (vc.producer_act) return fail(p, MG_ERR_UNSUPPORTED, "layer %d: attention after an activation", i);
+        Node n;
+        n.kind = NK_ATTN;
+        n.layer = i;
+        n.in = cur;
+        n.nh = l.n_heads;
+        n.dh = l.head_dim;
+        n.S = l.seq_len;
+        int ni = (int)p->nodes.size();
+        n.out = new_value(l.n_heads * l.head_dim, ni);
+        p->values[n.in].consumers++;
+        p->nodes.push_back(n);
+        cur = n.out;
+        break;
+      }
+      default:
+        return fail(p, MG_ERR_INVALID_ARG, "layer %d: unknown op %d", i, l.op);
+    }
+  }
+  if (!skips.empty()) return fail(p, MG_ERR_INVALID_ARG, "residual begin without end");
+  if (p->nodes.empty()) return fail(p, MG_ERR_INVALID_ARG, "graph has no computing layer");
+  if (p->values[cur].producer_act)
+    return fail(p, MG_ERR_UNSUPPORTED, "an activation directly before the loss is not supported");
+  for (auto& v : p->values)
+    if (v.consumers > 1) return fail(p, MG_ERR_UNSUPPORTED, "a value feeds two layers");
+  p->final_value = cur;
+  p->n_params = round_up(poff, kAlignElems);
+  if (p->p_off.empty()) return fail(p, MG_ERR_INVALID_ARG, "graph has no parameters");
+  if (p->dt == DT_BF16 && p->values[0].width % 8)
+    return fail(p, MG_ERR_ALIGN, "bf16 input rows must be a multiple of 16 bytes");
+
+  // which values need a gradient: anything downstream of a parameter
+  for (size_t ni = 0; ni < p->nodes.size(); ++ni) {
+    const Node& n = p->nodes[ni];
+    bool need = n.kind != NK_ATTN || p->values[n.in].need_grad;
+    if (n.skip >= 0 && p->values[n.skip].need_grad) need = true;
+    p->values[n.out].need_grad = need;
+    if (n.skip >= 0) p->values[n.skip].pending_add = n.out;
+  }
+  return MG_OK;
+}
+
+void layout_workspace(mg_plan* p) {
+  Bump b;
+  const size_t es = dtype_size(p->dt);
+  const size_t B = (size_t)p->batch;
+  for (size_t i = 1; i < p->values.size(); ++i) {
+    Value& v = p->values[i];
+    v.off = b.take(B * v.width * es);
+    if (v.need_grad) {
+      v.goff = b.take(B * v.width * es);
+      v.has_grad = true;
+    }
+  }
+  // x's gradient is never formed; a value's need_grad is false for x
+  for (Node& n : p->nodes) {
+    if (n.kind == NK_RMSNORM) n.rstd_off = b.take(B * 4);
+    if (n.kind == NK_ATTN) {
+      n.lse_off = b.take(B * n.nh * 4);
+      n.dsum_off = b.take(B * n.nh * 4);
+    }
+  }
+  if (p->dt == DT_BF16) p->shadow_off = b.take(p->n_params * 2);
+  // chunks
+  p->n_chunks = 0;
+  for (size_t t = 0; t < p->p_off.size(); ++t) {
+    size_t len = (size_t)p->p_rows[t] * p->p_cols[t];
+    p->n_chunks += (int)((len + kChunk - 1) / kChunk);
+  }
+  p->chunks_off = b.take(sizeof(Chunk) * (size_t)p->n_chunks);
+  p->loss_off = b.take(16);
+  p->flag_off = b.take(16);
+  p->rowloss_off = b.take(B * 4);
+  size_t maxw = 0;
+  for (auto& v : p->values) maxw = v.width > (int)maxw ? v.width : maxw;
+  size_t part = (size_t)kRowChunks * maxw * 4;
+  if (part < (size_t)kMsePartials * 4) part = (size_t)kMsePartials * 4;
+  p->partial_off = b.take(part);
+  p->ws_bytes = round_up(b.top, kWsAlign);
+}
+
+std::vector<Chunk> chunk_table(const mg_plan* p) {
+  std::vector<Chunk> t;
+  for (size_t i = 0; i < p->p_off.size(); ++i) {
+    size_t len = (size_t)p->p_rows[i] * p->p_cols[i];
+    for (size_t s = 0; s < len; s += kChunk) {
+      Chunk c;
+      c.start = (long long)(p->p_off[i] + s);
+      c.len = (int)(len - s < (size_t)kChunk ? len - s : kChunk);
+      c.shadow = p->p_is_weight[i];
+      t.push_back(c);
+    }
+  }
+  return t;
+}
+
+void build_dump(mg_plan* p) {
+  std::string s;
+  char b[256];
+  snprintf(b, sizeof b, "plan: batch %d, %s, %s, loss %d, %zu params, workspace %zu bytes\n",
+           p->batch, p->dt == DT_BF16 ? "bf16" : "strict-f32",
+           p->optimizer == MG_OPT_ADAM ? "adam" : "sgd", p->loss, p->n_params, p->ws_bytes);
+  s += b;
+  for (size_t i = 0; i < p->p_off.size(); ++i) {
+    snprintf(b, sizeof b, "  param %zu: offset %zu [%d x %d]\n", i, p->p_off[i], p->p_rows[i],
+             p->p_cols[i]);
+    s += b;
+  }
+  for (size_t i = 0; i < p->values.size(); ++i) {
+    const Value& v = p->values[i];
+    snprintf(b, sizeof b, "  value %zu: width %d at ws+%zu%s grad %s\n", i, v.width,
+             i == 0 ? (size_t)0 : v.off, i == 0 ? " (caller's x)" : "",
+             v.has_grad ? std::to_string(v.goff).c_str() : "-");
+    s += b;
+  }
+  for (size_t i = 0; i < p->sites.size(); ++i) {
+    snprintf(b, sizeof b, "  kernel %zu: %s  (%.3g flop, %.3g B)\n", i, p->sites[i].name.c_str(),
+             p->sites[i].flops, p->sites[i].bytes);
+    s += b;
+  }
+  p->dump = s;
+}
+
+mg_status check_device(mg_plan* p) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(p, e, "cudaGetDevice");
+  if (dev != p->device)
+    return fail(p, MG_ERR_INVALID_ARG, "plan belongs to device %d but device %d is current", p->device, dev);
+  return MG_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
+  if (!out) return fail(nullptr, MG_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!desc) return fail(nullptr, MG_ERR_INVALID_ARG, "desc is NULL");
+  mg_plan* p = new (std::nothrow) mg_plan();
+  if (!p) return fail(nullptr, MG_ERR_OOM, "host allocation failed");
+  mg_status st = compile(p, desc);
+  if (st != MG_OK) {
+    fail(nullptr, st, "%s", p->err.c_str());
+    delete p;
+    return st;
+  }
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e != cudaSuccess) {
+    mg_status r = cuda_fail(nullptr, e, "cudaGetDevice");
+    delete p;
+    return r;
+  }
+  layout_workspace(p);
+  e = cudaMalloc((void**)&p->ws, p->ws_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    mg_status r = fail(nullptr, MG_ERR_OOM, "workspace of %zu bytes: %s", p->ws_bytes, cudaGetErrorString(e));
+    p->ws = nullptr;
+    delete p;
+    return r;
+  }
+  std::vector<Chunk> ch = chunk_table(p);
+  e = cudaMemcpy(p->ws + p->chunks_off, ch.data(), ch.size() * sizeof(Chunk), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(p->ws + p->loss_off, 0, 16);
+  if (e != cudaSuccess) {
+    mg_status r = cuda_fail(nullptr, e, "workspace init");
+    cudaFree(p->ws);
+    delete p;
+    return r;
+  }
+  // register the schedule's kernels (dry run: no launches)
+  Exec ex{p, nullptr, true, false};
+  train_schedule(ex, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, 1);
+  build_dump(p);
+  *out = p;
+  return MG_OK;
+}
+
+void mg_step_plan_destroy(mg_plan* p) {
+  if (!p) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  for (auto ev : p->events) cudaEventDestroy(ev);
+  if (p->ws) cudaFree(p->ws);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete p;
+}
+
+size_t mg_param_count(const mg_plan* p) { return p ? p->n_params : 0; }
+
+int mg_param_tensor_count(const mg_plan* p) { return p ? (int)p->p_off.size() : 0; }
+
+mg_status mg_param_info(const mg_plan* p, int i, size_t* offset, int* rows, int* cols) {
+  if (!p) return fail(nullptr, MG_ERR_INVALID_ARG, "plan is NULL");
+  if (i < 0 || i >= (int)p->p_off.size())
+    return fail(const_cast<mg_plan*>(p), MG_ERR_INVALID_ARG, "tensor index %d out of range", i);
+  if (offset) *offset = p->p_off[i];
+  if (rows) *rows = p->p_rows[i];
+  if (cols) *cols = p->p_cols[i];
+  return MG_OK;
+}
+
+size_t mg_workspace_bytes(const mg_plan* p) { return p ? p->ws_bytes : 0; }
+
+mg_status mg_forward(mg_plan* p, const float* params, const void* x, float* out, mg_stream_t stream) {
+  if (!p) return fail(nullptr, MG_ERR_INVALID_ARG, "plan is NULL");
+  if (!params || !x || !out) return fail(p, MG_ERR_INVALID_ARG, "params, x and out must be non-NULL");
+  if (!aligned16(params) || !aligned16(x) || !aligned16(out))
+    return fail(p, MG_ERR_ALIGN, "params, x and out must be 16-byte aligned");
+  mg_status st = check_device(p);
+  if (st != MG_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(p, e, "earlier CUDA error");
+  Exec ex{p, s, false, false};
+  if (p->dt == DT_BF16) {
+    site(ex, "cast_bf16_weights", 0, p->n_params * 6.0, 1, [&] {
+      return cast_shadow(wsp<Chunk>(p, p->chunks_off), p->n_chunks, params, p->ws + p->shadow_off, s);
+    });
+    p->last_params = params;
+  }
+  forward_pass(ex, params, x);
+  const Value& f = p->values[p->final_value];
+  site(ex, "output_to_f32", 0, 0, 1, [&] {
+    return cast_to_f32(p->dt, p->ws + f.off, out, (size_t)p->batch * f.width, s);
+  });
+  p->last_launches = ex.launches;
+  if (ex.err != cudaSuccess) return cuda_fail(p, ex.err, "mg_forward launch");
+  return MG_OK;
+}
+
+mg_status mg_train_step(mg_plan* p, float* params, float* grads, float* adam_m, float* adam_v,
+                        const void* x, const void* labels, float lr, int step, mg_stream_t stream) {
+  if (!p) return fail(nullptr, MG_ERR_INVALID_ARG, "plan is NULL");
+  if (!params || !grads || !x || !labels)
+    return fail(p, MG_ERR_INVALID_ARG, "params, grads, x and labels must be non-NULL");
+  if (p->optimizer == MG_OPT_ADAM && (!adam_m || !adam_v))
+    return fail(p, MG_ERR_INVALID_ARG, "Adam needs adam_m and adam_v");
+  if (p->optimizer == MG_OPT_ADAM && step < 1) return fail(p, MG_ERR_INVALID_ARG, "step must be >= 1");
+  if (!aligned16(params) || !aligned16(grads) || !aligned16(x) || !aligned16(labels) ||
+      (adam_m && !aligned16(adam_m)) || (adam_v && !aligned16(adam_v)))
+    return fail(p, MG_ERR_ALIGN, "buffers must be 16-byte aligned");
+  const size_t nb = p->n_params * sizeof(float);
+  const char *pa = (const char*)params, *ga = (const char*)grads;
+  if (pa < ga + nb && ga < pa + nb) return fail(p, MG_ERR_INVALID_ARG, "grads must not alias params");
+  if (!(std::isfinite(lr))) return fail(p, MG_ERR_INVALID_ARG, "lr is not finite");
+  mg_status st = check_device(p);
+  if (st != MG_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(p, e, "earlier CUDA error");
+  int extra = 0;
+  if (p->dt == DT_BF16 && (step == 1 || params != p->last_params)) {
+    e = cast_shadow(wsp<Chunk>(p, p->chunks_off), p->n_chunks, params, p->ws + p->shadow_off, s);
+    if (e != cudaSuccess) return cuda_fail(p, e, "weight cast");
+    extra = 1;
+  }
+  p->last_params = params;
+  Exec ex{p, s, false, true};
+  ex.launches = extra;
+  train_schedule(ex, params, grads, adam_m, adam_v, x, labels, lr, step);
+  if (p->profiling && p->prof_calls < p->prof_max) p->prof_calls++;
+  p->last_launches = ex.launches;
+  if (ex.err != cudaSuccess) return cuda_fail(p, ex.err, "mg_train_step launch");
+  return MG_OK;
+}
+
+mg_status mg_loss(mg_plan* p, float* host_loss, mg_stream_t stream) {
+  if (!p || !host_loss) return fail(p, MG_ERR_INVALID_ARG, "plan and host_loss must be non-NULL");
+  cudaError_t e = cudaMemcpyAsync(host_loss, p->ws + p->loss_off, sizeof(float), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "mg_loss");
+  return MG_OK;
+}
+
+const float* mg_loss_device_ptr(const mg_plan* p) {
+  return p ? reinterpret_cast<const float*>(p->ws + p->loss_off) : nullptr;
+}
+
+mg_status mg_refresh_params(mg_plan* p, const float* params, mg_stream_t stream) {
+  if (!p || !params) return fail(p, MG_ERR_INVALID_ARG, "plan and params must be non-NULL");
+  if (!aligned16(params)) return fail(p, MG_ERR_ALIGN, "params must be 16-byte aligned");
+  if (p->dt != DT_BF16) return MG_OK;
+  cudaError_t e = cast_shadow(wsp<Chunk>(p, p->chunks_off), p->n_chunks, params, p->ws + p->shadow_off,
+                              (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "mg_refresh_params");
+  p->last_params = params;
+  return MG_OK;
+}
+
+size_t mg_plan_dump(const mg_plan* p, char* buf, size_t cap) {
+  if (!p) return 0;
+  if (buf && cap) {
+    size_t n = p->dump.size() < cap - 1 ? p->dump.size() : cap - 1;
+    memcpy(buf, p->dump.data(), n);
+    buf[n] = 0;
+  }
+  return p->dump.size();
+}
+
+const char* mg_last_error(const mg_plan* p) {
+  if (p) return p->err.c_str();
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  return g_err.c_str();
+}
+
+mg_status mg_debug_check_finite(mg_plan* p, const float* data, size_t n, long long* first_bad,
+                                mg_stream_t stream) {
+  if (!p || !data) return fail(p, MG_ERR_INVALID_ARG, "plan and data must be non-NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned long long* flag = wsp<unsigned long long>(p, p->flag_off);
+  unsigned long long h = ~0ull;
+  cudaError_t e = cudaMemcpyAsync(flag, &h, sizeof h, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = find_nonfinite(data, n, flag, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, flag, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(p, e, "mg_debug_check_finite");
+  if (first_bad) *first_bad = h == ~0ull ? -1 : (long long)h;
+  if (h != ~0ull) return fail(p, MG_ERR_NONFINITE, "non-finite value at index %llu", h);
+  return MG_OK;
+}
+
+int mg_last_launch_count(const mg_plan* p) { return p ? p->last_launches : 0; }
+
+mg_status mg_profile_begin(mg_plan* p, int max_calls) {
+  if (!p || max_calls <= 0) return fail(p, MG_ERR_INVALID_ARG, "bad profile request");
+  for (auto ev : p->events) cudaEventDestroy(ev);
+  p->events.assign((size_t)max_calls * p->sites.size() * 2, nullptr);
+  for (auto& ev : p->events) {
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaEventCreate");
+  }
+  for (auto& s : p->sites) {
+    s.launches = 0;
+    s.total_ms = 0;
+  }
+  p->profiling = true;
+  p->prof_max = max_calls;
+  p->prof_calls = 0;
+  return MG_OK;
+}
+
+mg_status mg_profile_end(mg_plan* p) {
+  if (!p || !p->profiling) return fail(p, MG_ERR_INVALID_ARG, "profiling not active");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(p, e, "mg_profile_end");
+  const size_t ns = p->sites.size();
+  for (int c = 0; c < p->prof_calls; ++c)
+    for (size_t i = 0; i < ns; ++i) {
+      float ms = 0;
+      if (cudaEventElapsedTime(&ms, p->events[(c * ns + i) * 2], p->events[(c * ns + i) * 2 + 1]) ==
+          cudaSuccess) {
+        p->sites[i].launches++;
+        p->sites[i].total_ms += ms;
+      } else {
+        cudaGetLastError();
+      }
+    }
+  p->profiling = false;
+  return MG_OK;
+}
+
+int mg_profile_entries(const mg_plan* p) { return p ? (int)p->sites.size() : 0; }
+
+mg_status mg_profile_entry(const mg_plan* p, int i, char* name, size_t name_cap, int* launches,
+                           double* total_ms, double* flops, double* bytes) {
+  if (!p || i < 0 || i >= (int)p->sites.size()) return fail(const_cast<mg_plan*>(p), MG_ERR_INVALID_ARG, "bad entry");
+  const Site& s = p->sites[i];
+  if (name && name_cap) {
+    size_t n = s.name.size() < name_cap - 1 ? s.name.size() : name_cap - 1;
+    memcpy(name, s.name.data(), n);
+    name[n] = 0;
+  }
+  if (launches) *launches = s.launches;
+  if (total_ms) *total_ms = s.total_ms;
+  if (flops) *flops = s.flops;
+  if (bytes) *bytes = s.bytes;
+  return MG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+"""Runs a workload through the library (via the C ABI) and through the oracle
+on the same seeded inputs, and compares them with the parity gates:
+
+* strict f32: max|a-b| / max|b| <= 1e-4 on the loss, every gradient tensor and
+  every updated parameter tensor, at every step;
+* bf16: loss relative error <= 1e-2 and per-tensor gradient cosine >= 0.999;
+  updated parameters within the largest distance one Adam step from the same
+  state can separate them (adam_step_bound).
+
+Both compare at every step from the oracle's own state (teacher forcing, see
+compare), so that rounding-level differences cannot accumulate into diverging
+trajectories; the free-running loss curve is checked as well.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from static_graph_nn_gb300 import Plan
+from static_graph_nn_gb300 import workloads as W
+
+STRICT_TOL = 1e-4
+BF16_LOSS_TOL = 1e-2
+BF16_COSINE = 0.999
+
+
+def to_device_inputs(w, precision):
+    x = W.make_x(w)
+    y = W.make_labels(w)
+    xt = torch.from_numpy(x).cuda()
+    if precision == "bf16":
+        xt = xt.to(torch.bfloat16)
+    yt = torch.from_numpy(y).cuda()
+    if w.loss == "mse" and precision == "bf16":
+        yt = yt.to(torch.bfloat16)
+    return x, y, xt.contiguous(), yt.contiguous()
+
+
+def pack(plan, tensors):
+    flat = torch.zeros(plan.param_count, dtype=torch.float32)
+    for (off, r, c), t in zip(plan.param_info(), tensors):
+        flat[off:off + r * c] = torch.from_numpy(np.ascontiguousarray(t, np.float32).reshape(-1))
+    return flat.cuda()
+
+
+def unpack(plan, flat, shapes):
+    f = flat.detach().cpu().numpy()
+    return [f[off:off + r * c].reshape(s).astype(np.float64)
+            for (off, r, c), (_, s) in zip(plan.param_info(), shapes)]
+
+
+class Device:
+    """Flat device buffers of one plan, loaded from / read back to per-tensor arrays."""
+
+    def __init__(self, plan, w, precision):
+        self.plan, self.w = plan, w
+        self.shapes = W.param_shapes(w.layers)
+        n = plan.param_count
+        self.params = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.grads = torch.zeros_like(self.params)
+        self.m = torch.zeros_like(self.params) if w.optimizer == "adam" else None
+        self.v = torch.zeros_like(self.params) if w.optimizer == "adam" else None
+
+    def load(self, params, m=None, v=None):
+        self.params.copy_(pack(self.plan, params))
+        if self.m is not None:
+            self.m.copy_(pack(self.plan, m if m is not None else [np.zeros_like(a) for a in params]))
+            self.v.copy_(pack(self.plan, v if v is not None else [np.zeros_like(a) for a in params]))
+        self.plan.refresh_params(self.params)
+
+    def read(self):
+        out = {"grads": unpack(self.plan, self.grads, self.shapes),
+               "params": unpack(self.plan, self.params, self.shapes)}
+        if self.m is not None:
+            out["adam_m"] = unpack(self.plan, self.m, self.shapes)
+            out["adam_v"] = unpack(self.plan, self.v, self.shapes)
+        return out
+
+
+def run_gpu(w, precision, steps, x=None, y=None):
+    """Free-running: the GPU's own trajectory from the initial parameters."""
+    plan = Plan.for_workload(w, precision)
+    x, y, xt, yt = to_device_inputs(w, precision)
+    dev = Device(plan, w, precision)
+    dev.load(W.init_params(w))
+    hist = []
+    for t in range(1, steps + 1):
+        plan.train_step(dev.params, dev.grads, dev.m, dev.v, xt, yt, w.lr, t)
+        r = dev.read()
+        r["loss"] = plan.loss()
+        hist.append(r)
+    torch.cuda.synchronize()
+    return plan, hist, (x, y)
+
+
+def max_rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def cosine(a, b):
+    a, b = a.reshape(-1), b.reshape(-1)
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))
+
+
+def update_band(w, p, g, m, v, t, dg):
+    """How far the oracle's own update of p moves when its gradient moves
+    anywhere within +-dg (sampled at 9 points): the part of an updated parameter
+    that the gradient gate leaves undetermined.  Near g = 0 Adam's normalised
+    step can take either sign."""
+    base = _oracle_update(w, p, g, m, v, t)
+    band = np.zeros_like(base)
+    for f in np.linspace(-1.0, 1.0, 9):
+        band = np.maximum(band, np.abs(_oracle_update(w, p, g + f * dg, m, v, t) - base))
+    return band
+
+
+def _oracle_update(w, p, g, m, v, t):
+    if w.optimizer == "sgd":
+        return oracle.sgd_update(p, g, w.lr).astype(np.float64)
+    return oracle.adam_update(p, g, m, v, w.lr, t, w.beta1, w.beta2, w.adam_eps)[0].astype(np.float64)
+
+
+def adam_step_bound(w):
+    """Largest |update| of one Adam step, elementwise: |m_hat| / sqrt(v_hat) is at
+    most (1-b1)/sqrt(1-b2) when (1-b1) > sqrt(1-b2), else 1 (Kingma & Ba, 2015,
+    section 2.1), so two runs from the same state differ by at most twice that."""
+    return 2.0 * w.lr * max(1.0, (1 - w.beta1) / math.sqrt(1 - w.beta2))
+
+
+def compare(w, precision, steps):
+    """Teacher-forced parity: at every step t the GPU starts from the oracle's
+    state after step t-1 (parameters, Adam moments) and must reproduce the
+    oracle's step t (loss, gradients, updated parameters and moments).  Then
+    the free-running GPU trajectory's loss curve must track the oracle's."""
+    x, y, xt, yt = to_device_inputs(w, precision)
+    p0 = W.init_params(w)
+    ho = oracle.run_steps(w.layers, p0, x, y, w.loss, precision, w.optimizer, w.lr, steps,
+                          w.beta1, w.beta2, w.adam_eps)
+    names = [n for n, _ in W.param_shapes(w.layers)]
+    plan = Plan.for_workload(w, precision)
+    dev = Device(plan, w, precision)
+    state = (p0, None, None)
+    worst = {"loss": 0.0, "grads": 0.0 if precision == "strict" else 1.0, "params": 0.0,
+             "curve": 0.0}
+    for t in range(1, steps + 1):
+        o = ho[t - 1]
+        dev.load(*state)
+        plan.train_step(dev.params, dev.grads, dev.m, dev.v, xt, yt, w.lr, t)
+        loss = plan.loss()
+        g = dev.read()
+        prev_p = state[0]
+        prev_m = state[1] if state[1] is not None else [np.zeros_like(a) for a in p0]
+        prev_v = state[2] if state[2] is not None else [np.zeros_like(a) for a in p0]
+        e = abs(loss - o["loss"]) / abs(o["loss"])
+        worst["loss"] = max(worst["loss"], e)
+        tol_loss = STRICT_TOL if precision == "strict" else BF16_LOSS_TOL
+        assert e <= tol_loss, f"step {t}: loss {loss} vs oracle {o['loss']}"
+        for i, n in enumerate(names):
+            a, b = g["grads"][i], o["grads"][i]
+            if precision == "strict":
+                e = max_rel(a, b)
+                worst["grads"] = max(worst["grads"], e)
+                assert e <= STRICT_TOL, f"step {t}: grad {n} max rel err {e:.3g}"
+                dg = STRICT_TOL * np.abs(b).max()
+                band = update_band(w, prev_p[i], b, prev_m[i], prev_v[i], t, dg)
+                pa, pb = g["params"][i], o["params"][i].astype(np.float64)
+                ulp = np.abs(pb) * 2.0 ** -22
+                excess = np.abs(pa - pb) - band - ulp
+                e = float(max(excess.max(), 0.0) / max(np.abs(pb).max(), 1e-30))
+                worst["params"] = max(worst["params"], e)
+                assert e <= STRICT_TOL, f"step {t}: param {n} max rel err {e:.3g} beyond band"
+                if w.optimizer == "adam":
+                    for key, bandk in (("adam_m", (1 - w.beta1) * dg),
+                                       ("adam_v", (1 - w.beta2) * (2 * np.abs(b) * dg + dg * dg))):
+                        ma, mb = g[key][i], o[key][i].astype(np.float64)
+                        excess = np.abs(ma - mb) - bandk - np.abs(mb) * 2.0 ** -22
+                        e = float(max(excess.max(), 0.0) / max(np.abs(mb).max(), 1e-30))
+                        assert e <= STRICT_TOL, f"step {t}: {key} {n} max rel err {e:.3g}"
+            else:
+                c = cosine(a, b)
+                worst["grads"] = min(worst["grads"], c)
+                assert c >= BF16_COSINE, f"step {t}: grad {n} cosine {c:.6f}"
+                d = float(np.abs(g["params"][i] - o["params"][i]).max())
+                bound = adam_step_bound(w) if w.optimizer == "adam" else 2 * w.lr * np.abs(b).max()
+                worst["params"] = max(worst["params"], d / bound)
+                assert d <= bound + 1e-6, f"step {t}: param {n} moved {d:.3g} from the oracle's"
+        state = (o["params"], o["adam_m"] or None, o["adam_v"] or None)
+    # free-running trajectory: loss curve
+    # (relative to the loss, floored at a tenth of the first step's loss: on a
+    # repeated batch the loss heads to 0, where a relative error means nothing)
+    _, hg, _ = run_gpu(w, precision, steps, x, y)
+    floor = 0.1 * abs(ho[0]["loss"])
+    for t, (a, b) in enumerate(zip(hg, ho)):
+        e = abs(a["loss"] - b["loss"]) / max(abs(b["loss"]), floor)
+        worst["curve"] = max(worst["curve"], e)
+        tol = STRICT_TOL if precision == "strict" else BF16_LOSS_TOL
+        assert e <= tol, f"free-running step {t + 1}: loss {a['loss']} vs oracle {b['loss']}"
+    plan.close()
+    return worst

@@ -60,14 +60,14 @@ def make_case(layers, rows, d_in, loss, seed=0):
 
 
 def loss_of(layers, params, x, y, loss):
-    out, _ = oracle.forward(layers, params, x, "strict")
+    out, _ = oracle.forward(layers, params, x, "exact")
     return oracle.loss_and_grad(loss, out, y)[0]
 
 
 def fd_error(layers, rows, d_in, loss, h=1e-6, seed=0):
     """max |analytic - central difference| / max |analytic| over all parameters."""
     params, x, y = make_case(layers, rows, d_in, loss, seed)
-    out, tape = oracle.forward(layers, params, x, "strict")
+    out, tape = oracle.forward(layers, params, x, "exact")
     _, dout = oracle.loss_and_grad(loss, out, y)
     grads, _ = oracle.backward(layers, params, tape, dout)
     worst = 0.0
@@ -285,7 +285,7 @@ def brute_force_mlp_232(seed=6, prec=40):
 
 def brute_force_error(seed=6):
     layers, params, x, y, loss, grads = brute_force_mlp_232(seed)
-    res = oracle.train_step(layers, params, x, y, "ce_dense", "strict", "sgd", 0.1, 1)
+    res = oracle.train_step(layers, params, x, y, "ce_dense", "exact", "sgd", 0.1, 1)
     err = abs(res["loss"] - loss) / abs(loss)
     for g, want in zip(res["grads"], grads):
         err = max(err, float(np.abs(g - want).max() / max(np.abs(want).max(), 1e-30)))
@@ -296,7 +296,7 @@ def loss_decrease_ok(seed=7):
     layers = [W.linear(6, 8, True), W.gelu_tanh(), W.linear(8, 4, True)]
     params, x, y = make_case(layers, 16, 6, "ce_dense", seed)
     hist = oracle.run_steps(layers, [p.astype(np.float32) for p in params], x, y,
-                            "ce_dense", "strict", "adam", 1e-2, 8)
+                            "ce_dense", "exact", "adam", 1e-2, 8)
     ls = [h["loss"] for h in hist]
     return all(b < a for a, b in zip(ls, ls[1:]))
 

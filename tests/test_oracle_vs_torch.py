@@ -27,7 +27,7 @@ def small(key):
     return w
 
 
-CASES = [(k, p) for k in SMALL for p in W.workload(k).precisions]
+CASES = [(k, p) for k in SMALL for p in ("exact",) + W.workload(k).precisions]
 
 
 @pytest.mark.parametrize("key,precision", CASES)

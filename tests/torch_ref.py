@@ -12,11 +12,40 @@ def bf16(t):
     return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
 
 
+def f32(t):
+    return t.to(torch.float32).to(torch.float64)
+
+
+class Store(torch.autograd.Function):
+    """A graph value in its storage type: rounds the value going forward and the
+    (summed) gradient with respect to it going backward."""
+
+    @staticmethod
+    def forward(ctx, t, precision):
+        ctx.precision = precision
+        return _round(t, precision)
+
+    @staticmethod
+    def backward(ctx, g):
+        return _round(g, ctx.precision), None
+
+
+def _round(t, precision):
+    if precision == "bf16":
+        return bf16(t)
+    if precision == "strict":
+        return f32(t)
+    return t
+
+
 def forward(layers, params, x, precision):
-    h = bf16(x) if precision == "bf16" else x
+    h = _round(x, precision)
     skips, i = [], 0
     for l in layers:
         op = l["op"]
+        if op == "residual_begin":
+            skips.append(h)
+            continue
         if op == "linear":
             w = params[i]
             i += 1
@@ -33,8 +62,6 @@ def forward(layers, params, x, precision):
         elif op == "rmsnorm":
             h = F.rms_norm(h, (l["d"],), weight=params[i], eps=l["eps"])
             i += 1
-        elif op == "residual_begin":
-            skips.append(h)
         elif op == "residual_end":
             h = skips.pop() + h
         elif op == "causal_attention":
@@ -45,6 +72,7 @@ def forward(layers, params, x, precision):
             sh = lambda t: t.reshape(nb, s, nh, dh).transpose(1, 2)  # noqa: E731
             o = F.scaled_dot_product_attention(sh(q), sh(k), sh(v), is_causal=True)
             h = o.transpose(1, 2).reshape(nb * s, d)
+        h = Store.apply(h, precision)
     return h
 
 
