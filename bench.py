@@ -1,0 +1,371 @@
+"""Benchmark: training steps/s and achieved TFLOP/s per step on one GB300.
+
+A step is one full training step of the workload (forward, loss, backward,
+optimizer) through the C ABI (libmg.so).  Default workload: the large GELU MLP
+(4096-4096-4096-4096-1000, batch 8192, bf16, Adam) -- the configuration the
+throughput target is quoted on.  ``--config`` selects another workload.
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the step has no exchange: replicas only), timing is the
+max over ranks, and ``value`` is the total steps/s of all ranks.
+
+``--impl reference`` times the CPU oracle (float64 numpy) on a bounded row
+sample of the same workload instead: the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (maximum SM clock)
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_for(key, precision):
+    from static_graph_nn_gb300 import workloads as W
+    w = W.workload(key)
+    if precision is None:
+        precision = "bf16" if "bf16" in w.precisions else w.precisions[0]
+    return w, precision
+
+
+def _oracle_inputs(w):
+    import numpy as np
+
+    from static_graph_nn_gb300 import workloads as W
+    p0 = W.init_params(w)
+    return p0, W.make_x(w), W.make_labels(w), [np.zeros_like(a) for a in p0]
+
+
+def _oracle_rows(w, rows, precision, inputs):
+    import oracle
+    p0, x, y, z = inputs
+    t0 = time.perf_counter()
+    oracle.train_step(w.layers, p0, x[:rows], y[:rows], w.loss, precision, w.optimizer, w.lr, 1,
+                      z, z, w.beta1, w.beta2, w.adam_eps)
+    return time.perf_counter() - t0
+
+
+def calibrate_rows(w, precision, inputs, target_s):
+    """Largest row sample (doubling, a multiple of the attention sequence) whose
+    oracle step stays near target_s seconds."""
+    unit = 1
+    for l in w.layers:
+        if l["op"] == "causal_attention":
+            unit = l["seq_len"]
+    rows = max(unit, min(w.batch, 32))
+    while rows < w.batch:
+        dt = _oracle_rows(w, rows, precision, inputs)
+        if dt * 2.2 > target_s:
+            break
+        rows = min(w.batch, rows * 2)
+    return rows
+
+
+def cpu_oracle_sample(w, precision, target_s=12.0):
+    """Times the oracle as it stands on a row sample of the workload.  Returns
+    (seconds per full step extrapolated by rows, rows sampled, threads)."""
+    inputs = _oracle_inputs(w)
+    rows = calibrate_rows(w, precision, inputs, target_s)
+    dt = _oracle_rows(w, rows, precision, inputs)
+    return dt * w.batch / rows, rows, os.cpu_count()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w, prec = workload_for(args.config, args.precision)
+    inputs = _oracle_inputs(w)
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = calibrate_rows(w, prec, inputs, per_step)
+    times = [_oracle_rows(w, rows, prec, inputs) * w.batch / rows
+             for _ in range(args.warmup + args.steps)]
+    sec = statistics.mean(times[args.warmup:] or times)
+    value = 1.0 / sec
+    flops = w.flops_per_step()
+    line = {
+        "impl": "reference", "metric": "training steps/s (achieved TFLOP/s per step)",
+        "value": value, "unit": "steps/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "precision": prec,
+                   "optimizer": w.optimizer},
+        "tflops": flops / sec / 1e12,
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"each step: the oracle on {rows} of {w.batch} rows, "
+                                   f"time scaled by rows"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--precision", default=None, choices=[None, "strict", "bf16"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from static_graph_nn_gb300 import Plan
+    from static_graph_nn_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    from static_graph_nn_gb300 import binding
+    binding.load()
+
+    w, prec = workload_for(args.config, args.precision)
+    plan = Plan.for_workload(w, prec)
+    p0 = W.init_params(w)
+    flat = torch.zeros(plan.param_count, dtype=torch.float32)
+    for (off, r, c), t in zip(plan.param_info(), p0):
+        flat[off:off + r * c] = torch.from_numpy(t.reshape(-1))
+    params = flat.cuda()
+    grads = torch.zeros_like(params)
+    m = torch.zeros_like(params) if w.optimizer == "adam" else None
+    v = torch.zeros_like(params) if w.optimizer == "adam" else None
+    x = W.make_x(w)
+    y = W.make_labels(w)
+    xt = torch.from_numpy(x)
+    if prec == "bf16":
+        xt = xt.to(torch.bfloat16)
+    yt = torch.from_numpy(y)
+    if w.loss == "mse" and prec == "bf16":
+        yt = yt.to(torch.bfloat16)
+    x_host = xt.contiguous().pin_memory()
+    y_host = yt.contiguous().pin_memory()
+    x_dev = x_host.cuda()
+    y_dev = y_host.cuda()
+    stream = torch.cuda.current_stream()
+    step = 0
+
+    def one_step():
+        nonlocal step
+        step += 1
+        plan.train_step(params, grads, m, v, x_dev, y_dev, w.lr, step, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs, per-kernel events ----
+    clocks = ClockSampler(local)
+    clocks.start()
+    plan.profile_begin(args.steps)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    prof = plan.profile_end()
+    clk = clocks.stop()
+    launches = plan.last_launch_count() * args.steps
+    loss = plan.loss(stream)
+
+    # ---- end to end: host buffers, H2D copies and the loss read inside ----
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)       # H2D of the step's inputs
+        y_dev.copy_(y_host, non_blocking=True)
+        one_step()
+        plan.loss(stream)                            # D2H of the loss (synchronises)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    ms_t = torch.tensor([ms], device="cuda")
+    e2e_t = torch.tensor([e2e_s], device="cuda")
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    e2e_s = float(e2e_t.item())
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    ms_step = ms / args.steps
+    flops = w.flops_per_step()
+    peaks, peak_src = load_peaks()
+    bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+
+    # dominant kernel (largest share of the timed region)
+    top = max(prof, key=lambda e: e["total_ms"])
+    avg_ms = top["total_ms"] / max(1, top["launches"])
+    if top["flops"] > 0:
+        if prec == "bf16":
+            bound, unit, peak = "tensor", "TFLOP/s", bf16_peak
+        else:
+            bound, unit, peak = "alu", "TFLOP/s", FP32_FFMA_TFLOPS
+        achieved = top["flops"] / (avg_ms * 1e-3) / 1e12
+    else:
+        bound, unit, peak = "hbm", "GB/s", hbm_peak
+        achieved = top["bytes"] / (avg_ms * 1e-3) / 1e9
+    total_prof = sum(e["total_ms"] for e in prof)
+    kernels = [{"name": e["name"], "share": e["total_ms"] / total_prof if total_prof else None,
+                "avg_ms": e["total_ms"] / max(1, e["launches"]),
+                "tflops": (e["flops"] / (e["total_ms"] / max(1, e["launches"]) * 1e-3) / 1e12)
+                if e["flops"] and e["total_ms"] else None,
+                "gbs": (e["bytes"] / (e["total_ms"] / max(1, e["launches"]) * 1e-3) / 1e9)
+                if e["total_ms"] else None}
+               for e in sorted(prof, key=lambda e: -e["total_ms"])[:8]]
+
+    value = world * 1e3 / ms_step
+    h2d = x_host.numel() * x_host.element_size() + y_host.numel() * y_host.element_size()
+    line = {
+        "metric": "training steps/s (achieved TFLOP/s per step)",
+        "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": prec if prec == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "precision": prec,
+                   "optimizer": w.optimizer, "flops_per_step": flops,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "working set per step >> 129 MB L2 (weights, activations, Adam state)"},
+        "tflops": flops / (ms_step * 1e-3) / 1e12,
+        "pct_of_peak": flops / (ms_step * 1e-3) / 1e12 / (bf16_peak if prec == "bf16" else FP32_FFMA_TFLOPS),
+        "peak_source": peak_src,
+        "roofline": {"kernel": top["name"], "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": None,
+                     "peak_note": f"{'sustained bf16' if bound == 'tensor' else bound} peak, {peak_src}"},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "loss": loss,
+        "clocks": clk,
+        "e2e": {"value": world / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4},
+        "plan_workspace_bytes": plan.workspace_bytes,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        sec, rows, threads = cpu_oracle_sample(w, prec)
+        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": "steps/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"one oracle step on {rows} of {w.batch} rows, "
+                                          f"time scaled by rows"}
+    print(json.dumps(line), flush=True)
+    plan.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
