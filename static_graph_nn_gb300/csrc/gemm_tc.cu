@@ -1,0 +1,442 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05) with TMA-fed
+// shared-memory stages, fp32 accumulators in tensor memory (TMEM) and the same
+// fused epilogue as the CUDA-core GEMM.  This is the matmul archetype of the
+// Meganeura README ("Why Meganeura" section) on its reduced-precision path
+// (Environment variables section: validated f16/bf16 input tiles), and it
+// serves the forward, input-gradient and weight-gradient GEMMs of every layer:
+//   forward  Z  = X  W     A = X  [M,K] K-major,   B = W  [K,N] N-major
+//   dX       dH = dZ W^T   A = dZ [M,K] K-major,   B = W  [N,K] K-major
+//   dW       dW = X^T dZ   A = X  [K,M] M-major,   B = dZ [K,N] N-major
+//
+// One persistent CTA per SM, 192 threads in three roles:
+//   warp 0      TMA producer: loads 128xBK tiles of A and BNxBK tiles of B into
+//               a ring of shared-memory stages (128-byte swizzle);
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16) from
+//               one elected lane; tcgen05.commit frees each stage and
+//               publishes each finished accumulator;
+//   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread, bias,
+//               activation, derivative mask, residual, store to global.
+// Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap
+// the main loop of tile i+1.  Every mbarrier wait is bounded; on expiry the
+// kernel records the failure in an error word and unwinds instead of hanging.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mg {
+namespace {
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;              // 64 bf16 = 128 bytes = one swizzle row
+constexpr int TC_THREADS = 192;
+constexpr uint32_t kWaitLimit = 1u << 26;   // bounded spin (~seconds)
+
+struct TcParams {
+  GemmArgs g;
+  int tiles_m, tiles_n, k_blocks;
+  int* err;                            // set to 1 on a timed-out wait
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait for the phase with this parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
+// byte offsets (16-byte units), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, majorness,
+// N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <typename TO>
+__device__ __forceinline__ float round_value_tc(float v) {
+  return sizeof(TO) == 2 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
+// Epilogue of 32 consecutive columns of one row (same rounding points as the
+// CUDA-core GEMM's epilogue).
+template <typename TO>
+__device__ __forceinline__ void epilogue_row32(const GemmArgs& g, int m, int n0, float (&v)[32]) {
+  const bool full = n0 + 32 <= g.N;
+  const size_t rz = (size_t)m * g.ldz, rs = (size_t)m * g.lds, rr = (size_t)m * g.ldr;
+  const bf16* saved = static_cast<const bf16*>(g.saved);
+  const bf16* resid = static_cast<const bf16*>(g.resid);
+  bf16* outz = static_cast<bf16*>(g.out_z);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    if (!full && n >= g.N) break;
+    float x = v[j];
+    if (g.bias) x += g.bias[n];
+    if (g.act || g.resid || g.out_z) x = round_value_tc<TO>(x);
+    if (outz) outz[rz + n] = __float2bfloat16_rn(x);
+    if (g.act) x = apply_act(g.act, x);
+    if (g.dact) {
+      x = round_value_tc<TO>(x);
+      x *= act_grad_from_saved(g.dact, __bfloat162float(saved[rs + n]));
+    }
+    if (resid) x += __bfloat162float(resid[rr + n]);
+    v[j] = x;
+  }
+  TO* out = static_cast<TO*>(g.out) + (size_t)m * g.ldo + n0;
+  if (full && sizeof(TO) == 2 && ((g.ldo & 7) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 pk;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[q * 8 + 0], v[q * 8 + 1]);
+      __nv_bfloat162 h1 = __floats2bfloat162_rn(v[q * 8 + 2], v[q * 8 + 3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[q * 8 + 4], v[q * 8 + 5]);
+      __nv_bfloat162 h3 = __floats2bfloat162_rn(v[q * 8 + 6], v[q * 8 + 7]);
+      pk.x = *reinterpret_cast<uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<uint32_t*>(&h1);
+      pk.z = *reinterpret_cast<uint32_t*>(&h2);
+      pk.w = *reinterpret_cast<uint32_t*>(&h3);
+      reinterpret_cast<uint4*>(out)[q] = pk;
+    }
+  } else if (full && sizeof(TO) == 4 && ((g.ldo & 3) == 0)) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      reinterpret_cast<float4*>(out)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+  } else {
+    for (int j = 0; j < 32 && n0 + j < g.N; ++j) st_elem(out, j, v[j]);
+  }
+}
+
+template <int BN, int STAGES, typename TO, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams P) {
+  constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+  constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+  constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned stage ring
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = P.tiles_m * P.tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+        const int m0 = (tile / P.tiles_n) * TC_BM, n0 = (tile % P.tiles_n) * BN;
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
+          mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          const int k0 = kb * TC_BK;
+          uint8_t* a = sA + stage * A_BYTES;
+          uint8_t* b = sB + stage * B_BYTES;
+          if (A_MN) {   // [K rows][M]: boxes of 64 M x BK rows
+#pragma unroll
+            for (int i = 0; i < TC_BM / 64; ++i) tma_load_2d(a + i * 64 * TC_BK * 2, &tmA, &full[stage], m0 + i * 64, k0);
+          } else {      // [M rows][K]: one box of 128 rows x 64 K
+            tma_load_2d(a, &tmA, &full[stage], k0, m0);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(b + i * 64 * TC_BK * 2, &tmB, &full[stage], n0 + i * 64, k0);
+          } else {
+            tma_load_2d(b, &tmB, &full[stage], k0, n0);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc(TC_BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(&tempty[acc], use ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < P.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            const uint64_t ad = A_MN ? smem_desc(a + k * 2048, 64 * TC_BK * 2, 1024)
+                                     : smem_desc(a + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc(b + k * 2048, 64 * TC_BK * 2, 1024)
+                                     : smem_desc(b + k * 32, 16, 1024);
+            mma_bf16(d, ad, bd, idesc, (kb | k) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);           // frees the stage when these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) { *abort_flag = 1; atomicExch(P.err, 1); break; }
+        mma_commit(&tfull[acc]);               // accumulator ready for the epilogue
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;              // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      if (!mbar_wait(&tfull[acc], use)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
+      if (*abort_flag) break;
+      tc_fence_after();
+      const int m0 = (tile / P.tiles_n) * TC_BM, n0 = (tile % P.tiles_n) * BN;
+      const int m = m0 + row_in_tile;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        if (m < P.g.M && n0 + c * 32 < P.g.N) epilogue_row32<TO>(P.g, m, n0 + c * 32, v);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows][cols] (cols contiguous, row stride ld elements), box
+// box_cols x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, long long rows, long long cols, long long ld,
+              int box_cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int BN, int STAGES, typename TO, bool A_MN, bool B_MN>
+cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  // A: logical [M, K].  K-major storage [M rows][K]; M-major storage [K rows][M].
+  bool ok = A_MN ? make_map(&ma, g.A, g.K, g.M, g.lda, 64, TC_BK)
+                 : make_map(&ma, g.A, g.M, g.K, g.lda, TC_BK, TC_BM);
+  // B: logical [K, N].  N-major storage [K rows][N]; K-major storage [N rows][K].
+  ok = ok && (B_MN ? make_map(&mb, g.B, g.K, g.N, g.ldb, 64, TC_BK)
+                   : make_map(&mb, g.B, g.N, g.K, g.ldb, TC_BK, BN));
+  if (!ok) return cudaErrorInvalidValue;
+  TcParams P;
+  P.g = g;
+  P.tiles_m = (g.M + TC_BM - 1) / TC_BM;
+  P.tiles_n = (g.N + BN - 1) / BN;
+  P.k_blocks = (g.K + TC_BK - 1) / TC_BK;
+  P.err = err;
+  const size_t smem = 1024 + (size_t)STAGES * (TC_BM + BN) * TC_BK * 2 + (2 * STAGES + 4) * 8 + 16;
+  auto kern = gemm_tc_kernel<BN, STAGES, TO, A_MN, B_MN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = P.tiles_m * P.tiles_n;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, TC_THREADS, smem, s>>>(ma, mb, P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_eligible(const GemmArgs& g) {
+  if (g.in_type != DT_BF16 || g.K <= 0) return false;
+  // TMA: 16-byte aligned bases and row strides
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al(g.A) || !al(g.B)) return false;
+  if ((g.lda * 2) % 16 || (g.ldb * 2) % 16) return false;
+  if (g.a_mn && g.b_k) return false;
+  if (g.out_type == DT_F32 && !g.a_mn) return false;   // only dW writes fp32
+  return encode_fn() != nullptr;
+}
+
+cudaError_t gemm_tc(const GemmArgs& g, int* err, cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if (g.a_mn) return launch_tc<256, 4, float, true, true>(g, err, s);   // dW (fp32 out)
+  if (g.b_k) return launch_tc<256, 4, bf16, false, false>(g, err, s);   // dX
+  return launch_tc<256, 4, bf16, false, true>(g, err, s);                // forward
+}
+
+}  // namespace mg

@@ -32,6 +32,10 @@ struct GemmArgs {
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
+// tcgen05/TMA version for bf16 operands whose rows are 16-byte aligned.
+// *err is set to 1 if a bounded pipeline wait expires.
+bool gemm_tc_eligible(const GemmArgs& g);
+cudaError_t gemm_tc(const GemmArgs& g, int* err, cudaStream_t s);
 
 // ---- loss ------------------------------------------------------------------
 // Softmax cross-entropy over rows of logits[B, C] (stride ld).  label_kind 0:

@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -100,6 +101,7 @@ struct mg_plan {
          flag_off = 0;
   int n_chunks = 0;
   const float* last_params = nullptr;
+  bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
   // schedule bookkeeping
   std::vector<Site> sites;
   int last_launches = 0;
@@ -196,12 +198,20 @@ double gemm_bytes(const GemmArgs& g) {
   return b;
 }
 
-cudaError_t run_gemm(const GemmArgs& g, cudaStream_t s) { return gemm_simt(g, s); }
+bool tc_path(const mg_plan* p, const GemmArgs& g) { return p->use_tc && gemm_tc_eligible(g); }
 
-std::string gemm_name(const char* what, int layer, const GemmArgs& g) {
+// error word of the tensor-core pipeline: 4 bytes after the loss scalar
+int* err_word(mg_plan* p) { return reinterpret_cast<int*>(p->ws + p->loss_off + 4); }
+
+cudaError_t run_gemm(mg_plan* p, const GemmArgs& g, cudaStream_t s) {
+  if (tc_path(p, g)) return gemm_tc(g, err_word(p), s);
+  return gemm_simt(g, s);
+}
+
+std::string gemm_name(const mg_plan* p, const char* what, int layer, const GemmArgs& g) {
   char b[160];
-  snprintf(b, sizeof b, "%s[l%d] %dx%dx%d %s", what, layer, g.M, g.N, g.K,
-           g.in_type == DT_BF16 ? "bf16" : "f32-ffma");
+  const char* kind = g.in_type != DT_BF16 ? "f32-ffma" : (tc_path(p, g) ? "bf16-tcgen05" : "bf16-simt");
+  snprintf(b, sizeof b, "%s[l%d] %dx%dx%d %s", what, layer, g.M, g.N, g.K, kind);
   return b;
 }
 
@@ -224,8 +234,8 @@ void forward_pass(Exec& e, const float* params, const void* x) {
       if (n.skip >= 0) { g.resid = val_ptr(p, n.skip, x); g.ldr = n.d_out; }
       g.aux_type = dt;
       g.out = p->ws + p->values[n.out].off; g.ldo = n.d_out; g.out_type = dt;
-      site(e, gemm_name("fwd", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
-           [&] { return run_gemm(g, e.s); });
+      site(e, gemm_name(p, "fwd", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+           [&] { return run_gemm(p, g, e.s); });
     } else if (n.kind == NK_RMSNORM) {
       double bytes = 2.0 * dtype_size(dt) * p->batch * n.d + 4.0 * n.d + 4.0 * p->batch;
       char nm[96];
@@ -292,8 +302,8 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
       g.B = gy; g.ldb = n.d_out; g.b_k = 0;
       g.in_type = dt; g.aux_type = dt;
       g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
-      site(e, gemm_name("dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
-           [&] { return run_gemm(g, e.s); });
+      site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+           [&] { return run_gemm(p, g, e.s); });
       if (n.has_bias) {
         char nm[96];
         snprintf(nm, sizeof nm, "db_colsum[l%d] %dx%d", n.layer, p->batch, n.d_out);
@@ -317,8 +327,8 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
         }
         if (dadd) { h.resid = dadd; h.ldr = n.d_in; }
         h.out = grad_ptr(p, n.in); h.ldo = n.d_in; h.out_type = dt;
-        site(e, gemm_name("dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
-             [&] { return run_gemm(h, e.s); });
+        site(e, gemm_name(p, "dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
+             [&] { return run_gemm(p, h, e.s); });
       }
     } else if (n.kind == NK_RMSNORM) {
       void* dx = vin.need_grad ? grad_ptr(p, n.in) : nullptr;
@@ -668,6 +678,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     delete p;
     return r;
   }
+  if (const char* ev = getenv("MG_GEMM")) p->use_tc = strcmp(ev, "simt") != 0;
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
   if (e != cudaSuccess) {
@@ -787,10 +798,16 @@ mg_status mg_train_step(mg_plan* p, float* params, float* grads, float* adam_m, 
 
 mg_status mg_loss(mg_plan* p, float* host_loss, mg_stream_t stream) {
   if (!p || !host_loss) return fail(p, MG_ERR_INVALID_ARG, "plan and host_loss must be non-NULL");
-  cudaError_t e = cudaMemcpyAsync(host_loss, p->ws + p->loss_off, sizeof(float), cudaMemcpyDeviceToHost,
+  struct { float loss; int err; } h = {0.f, 0};
+  cudaError_t e = cudaMemcpyAsync(&h, p->ws + p->loss_off, sizeof h, cudaMemcpyDeviceToHost,
                                   (cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(p, e, "mg_loss");
+  *host_loss = h.loss;
+  if (h.err) {
+    cudaMemsetAsync(err_word(p), 0, sizeof(int), (cudaStream_t)stream);
+    return fail(p, MG_ERR_TIMEOUT, "a tensor-core pipeline wait timed out; results are invalid");
+  }
   return MG_OK;
 }
 
