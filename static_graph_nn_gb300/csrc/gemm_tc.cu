@@ -35,6 +35,7 @@ constexpr uint32_t kWaitLimit = 1u << 26;   // bounded spin (~seconds)
 struct TcParams {
   GemmArgs g;
   int tiles_m, tiles_n, k_blocks;
+  int vec;                             // epilogue pointers/strides allow 16-byte vectors
   int* err;                            // set to 1 on a timed-out wait
 };
 
@@ -148,52 +149,106 @@ __device__ __forceinline__ float round_value_tc(float v) {
   return sizeof(TO) == 2 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
 
+__device__ __forceinline__ void load8_bf16(const bf16* p, float* f) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ void store8_bf16(bf16* p, const float* f) {
+  uint4 u;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
 // Epilogue of 32 consecutive columns of one row (same rounding points as the
-// CUDA-core GEMM's epilogue).
+// CUDA-core GEMM's epilogue).  Full, aligned chunks move in 16-byte vectors.
 template <typename TO>
-__device__ __forceinline__ void epilogue_row32(const GemmArgs& g, int m, int n0, float (&v)[32]) {
-  const bool full = n0 + 32 <= g.N;
+__device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int m, int n0,
+                                               float (&v)[32]) {
+  const bool full = vec && n0 + 32 <= g.N;
+  if (full) {
+    if (g.bias) {
+      const float4* b4 = reinterpret_cast<const float4*>(g.bias + n0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 b = b4[q];
+        v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
+      }
+    }
+    if (g.act || g.resid || g.out_z) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = round_value_tc<TO>(v[j]);
+    }
+    if (g.out_z) {
+      bf16* z = static_cast<bf16*>(g.out_z) + (size_t)m * g.ldz + n0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) store8_bf16(z + 8 * q, v + 8 * q);
+    }
+    if (g.act) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = apply_act(g.act, v[j]);
+    }
+    if (g.dact) {
+      const bf16* sv = static_cast<const bf16*>(g.saved) + (size_t)m * g.lds + n0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+        load8_bf16(sv + 8 * q, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[8 * q + i] = round_value_tc<TO>(v[8 * q + i]) * act_grad_from_saved(g.dact, f[i]);
+      }
+    }
+    if (g.resid) {
+      const bf16* rv = static_cast<const bf16*>(g.resid) + (size_t)m * g.ldr + n0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+        load8_bf16(rv + 8 * q, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * q + i] += f[i];
+      }
+    }
+    TO* out = static_cast<TO*>(g.out) + (size_t)m * g.ldo + n0;
+    if (sizeof(TO) == 2) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) store8_bf16(reinterpret_cast<bf16*>(out) + 8 * q, v + 8 * q);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(out)[q] =
+            make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+    }
+    return;
+  }
+  // ragged or unaligned chunk: element by element
   const size_t rz = (size_t)m * g.ldz, rs = (size_t)m * g.lds, rr = (size_t)m * g.ldr;
-  const bf16* saved = static_cast<const bf16*>(g.saved);
-  const bf16* resid = static_cast<const bf16*>(g.resid);
-  bf16* outz = static_cast<bf16*>(g.out_z);
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const int n = n0 + j;
-    if (!full && n >= g.N) break;
+    if (n >= g.N) continue;
     float x = v[j];
     if (g.bias) x += g.bias[n];
     if (g.act || g.resid || g.out_z) x = round_value_tc<TO>(x);
-    if (outz) outz[rz + n] = __float2bfloat16_rn(x);
+    if (g.out_z) static_cast<bf16*>(g.out_z)[rz + n] = __float2bfloat16_rn(x);
     if (g.act) x = apply_act(g.act, x);
     if (g.dact) {
       x = round_value_tc<TO>(x);
-      x *= act_grad_from_saved(g.dact, __bfloat162float(saved[rs + n]));
+      x *= act_grad_from_saved(g.dact, __bfloat162float(static_cast<const bf16*>(g.saved)[rs + n]));
     }
-    if (resid) x += __bfloat162float(resid[rr + n]);
-    v[j] = x;
-  }
-  TO* out = static_cast<TO*>(g.out) + (size_t)m * g.ldo + n0;
-  if (full && sizeof(TO) == 2 && ((g.ldo & 7) == 0)) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 pk;
-      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[q * 8 + 0], v[q * 8 + 1]);
-      __nv_bfloat162 h1 = __floats2bfloat162_rn(v[q * 8 + 2], v[q * 8 + 3]);
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[q * 8 + 4], v[q * 8 + 5]);
-      __nv_bfloat162 h3 = __floats2bfloat162_rn(v[q * 8 + 6], v[q * 8 + 7]);
-      pk.x = *reinterpret_cast<uint32_t*>(&h0);
-      pk.y = *reinterpret_cast<uint32_t*>(&h1);
-      pk.z = *reinterpret_cast<uint32_t*>(&h2);
-      pk.w = *reinterpret_cast<uint32_t*>(&h3);
-      reinterpret_cast<uint4*>(out)[q] = pk;
-    }
-  } else if (full && sizeof(TO) == 4 && ((g.ldo & 3) == 0)) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      reinterpret_cast<float4*>(out)[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
-  } else {
-    for (int j = 0; j < 32 && n0 + j < g.N; ++j) st_elem(out, j, v[j]);
+    if (g.resid) x += __bfloat162float(static_cast<const bf16*>(g.resid)[rr + n]);
+    st_elem(static_cast<TO*>(g.out), (size_t)m * g.ldo + n, x);
   }
 }
 
@@ -326,7 +381,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        if (m < P.g.M && n0 + c * 32 < P.g.N) epilogue_row32<TO>(P.g, m, n0 + c * 32, v);
+        if (m < P.g.M && n0 + c * 32 < P.g.N) epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -405,6 +460,12 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
   P.tiles_n = (g.N + BN - 1) / BN;
   P.k_blocks = (g.K + TC_BK - 1) / TC_BK;
   P.err = err;
+  {
+    auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
+    P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) &&
+            (lds & 7) == 0;
+  }
   const size_t smem = 1024 + (size_t)STAGES * (TC_BM + BN) * TC_BK * 2 + (2 * STAGES + 4) * 8 + 16;
   auto kern = gemm_tc_kernel<BN, STAGES, TO, A_MN, B_MN>;
   static bool attr_set = false;
