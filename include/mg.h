@@ -169,6 +169,33 @@ int mg_profile_entries(const mg_plan* plan);
 mg_status mg_profile_entry(const mg_plan* plan, int i, char* name, size_t name_cap,
                            int* launches, double* total_ms, double* flops, double* bytes);
 
+/* ---- softmax cross-entropy without device allocation -----------------
+ * The Meganeura pages have no counterpart to this call.  It is for callers
+ * that may not allocate device memory -- for example code running inside
+ * another framework's plugin or kernel-enqueue hook, or a process whose device
+ * memory is already reserved by its own caching allocator -- and therefore
+ * cannot create a plan, whose workspace mg_step_plan_create allocates.
+ *
+ * Computes the same softmax cross-entropy loss and gradient as the training
+ * step's loss kernel: for logits [rows, cols] row-major (dtype 0 = fp32,
+ * 1 = bf16), labels dense fp32 [rows, cols] (label_kind 0) or int32 class ids
+ * [rows] (label_kind 1), it writes dlogits (same dtype and layout as logits)
+ * = (softmax * sum(y) - y) / rows and *loss (one fp32, device memory) = the
+ * mean over rows of -sum_c y_c log softmax_c.  All pointers are caller-owned
+ * device memory; nothing is allocated, and no cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *
+ * Scratch: the per-row losses go to a fixed array in the library's device
+ * memory of 65536 floats (256 KB), held by every GPU that loads the library
+ * until the process exits.  rows above 65536 return MG_ERR_INVALID_ARG.  The
+ * first call on a device looks up that array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU (different streams, or
+ * different host threads) race and give wrong results.  Each call overwrites
+ * the slots it reads, so nothing needs clearing between calls. */
+mg_status mg_softmax_ce_noalloc(int dtype, const void* logits, int rows, int cols, int label_kind,
+                                const void* labels, void* dlogits, float* loss, mg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,8 @@ _SIGS = {
     "mg_profile_begin": (ctypes.c_int, [_P, ctypes.c_int]),
     "mg_profile_end": (ctypes.c_int, [_P]),
     "mg_profile_entries": (ctypes.c_int, [_P]),
+    "mg_softmax_ce_noalloc": (ctypes.c_int, [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, _P, _P, _P, _P]),
     "mg_profile_entry": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_char_p, ctypes.c_size_t,
                                         ctypes.POINTER(ctypes.c_int),
                                         ctypes.POINTER(ctypes.c_double),

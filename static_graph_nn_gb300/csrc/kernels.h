@@ -87,4 +87,7 @@ cudaError_t cast_to_f32(DType t, const void* src, float* dst, size_t n, cudaStre
 cudaError_t find_nonfinite(const float* data, size_t n, unsigned long long* first_bad,
                            cudaStream_t s);
 
+// Sets the process-wide message returned by mg_last_error(NULL).
+void set_global_error(const char* msg);
+
 }  // namespace mg

@@ -2,6 +2,9 @@
 // error (+ its gradient), the reduction archetype of the Meganeura README
 // (Example section: cross_entropy_loss(logits, labels) with a dense [B, C]
 // label tensor; "Why Meganeura" section: the reduction kernel archetype).
+#include <mutex>
+
+#include "../../include/mg.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -134,3 +137,74 @@ cudaError_t mse_loss(DType t, const void* o, const void* target, size_t n, void*
 }
 
 }  // namespace mg
+
+// ---------------------------------------------------------------------------
+// Softmax cross-entropy without any device allocation.
+//
+// For callers that are not allowed to allocate device memory -- code running
+// inside another framework's plugin or kernel-enqueue hook, or a process whose
+// device memory is already reserved by its own caching allocator -- and so
+// cannot create a plan (mg_step_plan_create allocates the plan's workspace).
+// The per-row losses that the plan keeps in its workspace live here in a
+// fixed file-scope device array instead.  Every GPU that loads the library
+// holds this array (kNoAllocMaxRows floats, 256 KB) until the process exits.
+namespace {
+
+constexpr int kNoAllocMaxRows = 65536;
+__device__ __align__(256) float g_noalloc_row_loss[kNoAllocMaxRows];
+
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 256;
+float* g_noalloc_scratch[kMaxDevices] = {};   // device address of the array, per device
+
+}  // namespace
+
+extern "C" mg_status mg_softmax_ce_noalloc(int dtype, const void* logits, int rows, int cols,
+                                           int label_kind, const void* labels, void* dlogits,
+                                           float* loss, mg_stream_t stream) {
+  using namespace mg;
+  if (!logits || !labels || !dlogits || !loss) {
+    set_global_error("mg_softmax_ce_noalloc: logits, labels, dlogits and loss must be non-NULL");
+    return MG_ERR_INVALID_ARG;
+  }
+  if ((dtype != 0 && dtype != 1) || (label_kind != 0 && label_kind != 1)) {
+    set_global_error("mg_softmax_ce_noalloc: dtype and label_kind must be 0 or 1");
+    return MG_ERR_INVALID_ARG;
+  }
+  if (rows < 1 || rows > kNoAllocMaxRows || cols < 1) {
+    set_global_error("mg_softmax_ce_noalloc: rows must be in [1, 65536] and cols >= 1");
+    return MG_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    set_global_error("mg_softmax_ce_noalloc: no usable current CUDA device");
+    return MG_ERR_CUDA;
+  }
+  float* scratch = nullptr;
+  {
+    // First call on this device: look up the array's device address (host
+    // code cannot use the array's name as a device pointer).
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_scratch[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_row_loss);
+      if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        set_global_error("mg_softmax_ce_noalloc: cudaGetSymbolAddress failed");
+        return MG_ERR_CUDA;
+      }
+      g_noalloc_scratch[dev] = static_cast<float*>(p);
+    }
+    scratch = g_noalloc_scratch[dev];
+  }
+  // Every row's slot is written before the reduction reads it, so the array
+  // needs no clearing between calls.
+  e = ce_loss(dtype == 1 ? DT_BF16 : DT_F32, logits, rows, cols, cols, label_kind, labels,
+              dlogits, scratch, loss, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    set_global_error("mg_softmax_ce_noalloc: kernel launch failed");
+    return MG_ERR_CUDA;
+  }
+  return MG_OK;
+}

@@ -657,6 +657,11 @@ mg_status check_device(mg_plan* p) {
 
 }  // namespace
 
+void mg::set_global_error(const char* msg) {
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  g_err = msg;
+}
+
 // ============================================================================
 extern "C" {
 
