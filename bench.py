@@ -43,6 +43,65 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries)
+    every ~2 ms from a background thread while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:   # NVML numbers GPUs on its own; match the CUDA device by PCI address
+            import torch
+            pr = torch.cuda.get_device_properties(gpu_index)
+            bus = b"%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            bus = None
+        if bus is None or self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(int(gpu_index), ctypes.byref(self.h)) != 0:
+                raise RuntimeError("no NVML handle")
+        self.samples, self.reasons = [], set()
+        self.stop_flag = False
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        clk, mx, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk))          # NVML_CLOCK_SM
+        self.max = self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx)) == 0 and mx.value
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if f(self.h, ct.byref(rs)) == 0:
+            for bit, name in self.REASONS.items():
+                if rs.value & bit:
+                    self.reasons.add(name)
+        self.samples.append(clk.value)
+
+    def _run(self):
+        while not self.stop_flag:
+            self._one()
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join(timeout=2)
+        self._one()
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max or None, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "nvml"}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -254,7 +313,10 @@ def main():
     torch.cuda.synchronize()
 
     # ---- timed region: device-resident inputs, per-kernel events ----
-    clocks = ClockSampler(local)
+    try:
+        clocks = NvmlSampler(local)
+    except Exception:
+        clocks = ClockSampler(local)
     clocks.start()
     plan.profile_begin(args.steps)
     if dist:

@@ -218,6 +218,53 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
   }
 }
 
+// Small or skinny GEMMs (few output tiles, e.g. 10 classes): one warp per
+// output element, lanes split K; the compensated variant combines the lanes'
+// (sum, error) pairs with TwoSum so the result stays correctly rounded.
+template <typename T, typename TO, typename TX, bool COMP>
+__global__ void __launch_bounds__(256) gemm_warp_kernel(const GemmArgs g) {
+  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (long long)g.M * g.N) return;          // whole warps only
+  const int m = (int)(wid / g.N), n = (int)(wid % g.N);
+  const T* A = static_cast<const T*>(g.A);
+  const T* B = static_cast<const T*>(g.B);
+  float s = 0.0f, c = 0.0f;
+  if (COMP && lane == 0 && g.bias) s = g.bias[n];
+  for (int k = lane; k < g.K; k += 32) {
+    float a = ld_elem(A, g.a_mn ? (size_t)k * g.lda + m : (size_t)m * g.lda + k);
+    float b = ld_elem(B, g.b_k ? (size_t)n * g.ldb + k : (size_t)k * g.ldb + n);
+    if (COMP)
+      dot2_step(a, b, s, c);
+    else
+      s = fmaf(a, b, s);
+  }
+  float v;
+  if (COMP) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float so = __shfl_xor_sync(0xffffffffu, s, off);
+      float co = __shfl_xor_sync(0xffffffffu, c, off);
+      float t = __fadd_rn(s, so);
+      float z = __fsub_rn(t, s);
+      float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(so, z));
+      s = t;
+      c = __fadd_rn(__fadd_rn(c, co), e);
+    }
+    v = __fadd_rn(s, c);
+  } else {
+    v = warp_sum(s);
+  }
+  if (lane == 0) epilogue_elem<TO, TX>(g, COMP ? nullptr : g.bias, m, n, v);
+}
+
+template <typename T, typename TO, typename TX, bool COMP>
+cudaError_t launch_warp(const GemmArgs& g, cudaStream_t s) {
+  long long threads = (long long)g.M * g.N * 32;
+  gemm_warp_kernel<T, TO, TX, COMP><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
 template <typename T, typename TO, typename TX, bool A_MN, bool B_K, bool COMP = false>
 cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
@@ -231,6 +278,14 @@ cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
 // B K-major), dW (A M-major, B N-major, fp32 output).
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if ((long long)g.M * g.N <= 65536 && g.K >= 64) {   // too few tiles: warp per output
+    if (g.in_type == DT_F32) {
+      if (!g.a_mn && !g.b_k) return launch_warp<float, float, float, true>(g, s);
+      return launch_warp<float, float, float, false>(g, s);
+    }
+    if (g.out_type == DT_F32) return launch_warp<bf16, float, bf16, false>(g, s);
+    return launch_warp<bf16, bf16, bf16, false>(g, s);
+  }
   if (g.in_type == DT_F32) {   // strict path: everything fp32
     if (!g.a_mn && !g.b_k) return launch1<float, float, float, false, false, true>(g, s);
     if (!g.a_mn && g.b_k) return launch1<float, float, float, false, true>(g, s);

@@ -81,6 +81,106 @@ __global__ void __launch_bounds__(256) ce_kernel(const T* logits, int C, long lo
   }
 }
 
+// bf16 logits whose rows are whole 16-byte vectors (C % 8 == 0): the same two
+// passes with 8 columns per access.
+template <bool DENSE>
+__global__ void __launch_bounds__(256) ce_kernel_vec(const bf16* logits, int C, long long ld,
+                                                     const void* labels, bf16* dlogits,
+                                                     float* row_loss, float inv_b) {
+  __shared__ float red[32];
+  __shared__ float sh_m, sh_s;
+  const int r = blockIdx.x;
+  const bf16* z = logits + (size_t)r * ld;
+  bf16* dz = dlogits + (size_t)r * ld;
+  const int nv = C >> 3;
+  float m = -INFINITY, s = 0.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    uint4 u = reinterpret_cast<const uint4*>(z)[v];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      x[2 * i] = t.x;
+      x[2 * i + 1] = t.y;
+    }
+    float vm = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) vm = fmaxf(vm, x[i]);
+    if (vm > m) {
+      s = (m == -INFINITY) ? 0.0f : s * expf(m - vm);
+      m = vm;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += expf(x[i] - m);
+  }
+  float bm = block_max(m, red);
+  float sc = (m == -INFINITY) ? 0.0f : s * expf(m - bm);
+  float bs = block_sum(sc, red);
+  if (threadIdx.x == 0) {
+    sh_m = bm;
+    sh_s = bs;
+  }
+  __syncthreads();
+  const float lse = sh_m + logf(sh_s);
+  float ysum = 1.0f, yz = 0.0f;
+  int t = -1;
+  const float* y = DENSE ? static_cast<const float*>(labels) + (size_t)r * C : nullptr;
+  if (DENSE) {
+    float a = 0.0f, b = 0.0f;
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float4 y0 = reinterpret_cast<const float4*>(y)[2 * v];
+      float4 y1 = reinterpret_cast<const float4*>(y)[2 * v + 1];
+      uint4 u = reinterpret_cast<const uint4*>(z)[v];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      float2 t0 = __bfloat1622float2(h[0]), t1 = __bfloat1622float2(h[1]);
+      float2 t2 = __bfloat1622float2(h[2]), t3 = __bfloat1622float2(h[3]);
+      a += y0.x + y0.y + y0.z + y0.w + y1.x + y1.y + y1.z + y1.w;
+      b += y0.x * t0.x + y0.y * t0.y + y0.z * t1.x + y0.w * t1.y + y1.x * t2.x + y1.y * t2.y +
+           y1.z * t3.x + y1.w * t3.y;
+    }
+    ysum = block_sum(a, red);
+    yz = block_sum(b, red);
+  } else {
+    t = static_cast<const int*>(labels)[r];
+  }
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    uint4 u = reinterpret_cast<const uint4*>(z)[v];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    float g[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 q = __bfloat1622float2(h[i]);
+      g[2 * i] = expf(q.x - lse);
+      g[2 * i + 1] = expf(q.y - lse);
+    }
+    if (DENSE) {
+      float4 y0 = reinterpret_cast<const float4*>(y)[2 * v];
+      float4 y1 = reinterpret_cast<const float4*>(y)[2 * v + 1];
+      const float yy[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = (g[i] * ysum - yy[i]) * inv_b;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = (g[i] - (v * 8 + i == t ? 1.0f : 0.0f)) * inv_b;
+    }
+    uint4 o;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 hh = __floats2bfloat162_rn(g[2 * i], g[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+    reinterpret_cast<uint4*>(dz)[v] = o;
+  }
+  if (threadIdx.x == 0) {
+    if (DENSE)
+      row_loss[r] = lse * ysum - yz;
+    else
+      row_loss[r] = (t >= 0 && t < C) ? lse - __bfloat162float(z[t]) : __int_as_float(0x7fc00000);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) mse_kernel(const T* o, const T* t, size_t n, T* dout,
                                                   float* partials, float two_over_n) {
@@ -110,6 +210,15 @@ cudaError_t ce_loss(DType t, const void* logits, int B, int C, long long ld, int
     else
       ce_kernel<float, false><<<B, 256, 0, s>>>((const float*)logits, C, ld, labels,
                                                 (float*)dlogits, row_loss, inv_b);
+  } else if (C % 8 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0 &&
+             (reinterpret_cast<uintptr_t>(dlogits) & 15) == 0 &&
+             (label_kind == 1 || (reinterpret_cast<uintptr_t>(labels) & 15) == 0)) {
+    if (label_kind == 0)
+      ce_kernel_vec<true><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels, (bf16*)dlogits,
+                                            row_loss, inv_b);
+    else
+      ce_kernel_vec<false><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels, (bf16*)dlogits,
+                                             row_loss, inv_b);
   } else {
     if (label_kind == 0)
       ce_kernel<bf16, true><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels,

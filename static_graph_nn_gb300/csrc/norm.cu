@@ -85,6 +85,125 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_kernel(
   }
 }
 
+// bf16 rows with d a multiple of 8: each thread owns 16-byte vectors (8
+// columns) v = tid, tid + 256, ... of every row it visits.
+constexpr int NV_MAX = 4;   // d <= 256 * 8 * 4 = 8192
+
+__device__ __forceinline__ void ld8(const bf16* p, float* f) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ void st8(bf16* p, const float* f) {
+  uint4 u;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_vec(const bf16* x, const float* gamma,
+                                                                bf16* y, float* rstd, int rows,
+                                                                int d, float eps) {
+  __shared__ float red[32];
+  const int nvec = d >> 3;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const bf16* xr = x + (size_t)r * d;
+    float v[NV_MAX][8];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV_MAX; ++i) {
+      int vi = threadIdx.x + i * NORM_THREADS;
+      if (vi < nvec) {
+        ld8(xr + vi * 8, v[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += v[i][j] * v[i][j];
+      }
+    }
+    ss = block_sum(ss, red);
+    const float rs = 1.0f / sqrtf(ss / (float)d + eps);
+    if (threadIdx.x == 0) rstd[r] = rs;
+    bf16* yr = y + (size_t)r * d;
+#pragma unroll
+    for (int i = 0; i < NV_MAX; ++i) {
+      int vi = threadIdx.x + i * NORM_THREADS;
+      if (vi < nvec) {
+        float o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = v[i][j] * rs * gamma[vi * 8 + j];
+        st8(yr + vi * 8, o);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, const bf16* x,
+                                                                const float* rstd,
+                                                                const float* gamma,
+                                                                const bf16* dadd, bf16* dx,
+                                                                float* dgamma_partials, int rows,
+                                                                int d) {
+  __shared__ float red[32];
+  const int nvec = d >> 3;
+  float dg[NV_MAX][8];
+#pragma unroll
+  for (int i = 0; i < NV_MAX; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dg[i][j] = 0.0f;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float rs = rstd[r];
+    float xv[NV_MAX][8], gv[NV_MAX][8];
+    float gx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV_MAX; ++i) {
+      int vi = threadIdx.x + i * NORM_THREADS;
+      if (vi < nvec) {
+        float dyv[8];
+        ld8(dy + (size_t)r * d + vi * 8, dyv);
+        ld8(x + (size_t)r * d + vi * 8, xv[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          gv[i][j] = dyv[j] * gamma[vi * 8 + j];
+          dg[i][j] += dyv[j] * xv[i][j] * rs;
+          gx += gv[i][j] * xv[i][j];
+        }
+      }
+    }
+    if (dx) {
+      gx = block_sum(gx, red) / (float)d;
+      const float k = rs * rs * gx;
+#pragma unroll
+      for (int i = 0; i < NV_MAX; ++i) {
+        int vi = threadIdx.x + i * NORM_THREADS;
+        if (vi < nvec) {
+          float o[8], a[8];
+          if (dadd) ld8(dadd + (size_t)r * d + vi * 8, a);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] = rs * (gv[i][j] - xv[i][j] * k) + (dadd ? a[j] : 0.0f);
+          st8(dx + (size_t)r * d + vi * 8, o);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NV_MAX; ++i) {
+    int vi = threadIdx.x + i * NORM_THREADS;
+    if (vi < nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dgamma_partials[(size_t)blockIdx.x * d + vi * 8 + j] = dg[i][j];
+    }
+  }
+}
+
 // partials[chunk, c] = sum of src[r, c] over the rows of this chunk.
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_pass1(const T* src, int rows, int cols, long long ld,
@@ -126,6 +245,11 @@ cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, flo
                         int d, float eps, cudaStream_t s) {
   if (d > NORM_THREADS * NORM_MAX_PER_THREAD) return cudaErrorInvalidValue;
   int grid = rows < 152 * 16 ? rows : 152 * 16;
+  if (t == DT_BF16 && d % 8 == 0 && d <= NORM_THREADS * 8 * NV_MAX &&
+      (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+    rmsnorm_fwd_vec<<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd, rows, d, eps);
+    return cudaGetLastError();
+  }
   if (t == DT_F32)
     rmsnorm_fwd_kernel<float><<<grid, NORM_THREADS, 0, s>>>((const float*)x, gamma, (float*)y,
                                                             rstd, rows, d, eps);
@@ -139,6 +263,15 @@ cudaError_t rmsnorm_bwd(DType t, const void* dy, const void* x, const float* rst
                         const float* gamma, const void* dadd, void* dx, float* dgamma_partials,
                         int row_chunks, float* dgamma, int rows, int d, cudaStream_t s) {
   if (d > NORM_THREADS * NORM_MAX_PER_THREAD) return cudaErrorInvalidValue;
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (t == DT_BF16 && d % 8 == 0 && d <= NORM_THREADS * 8 * NV_MAX && al(dy) && al(x) &&
+      al(dadd) && al(dx)) {
+    rmsnorm_bwd_vec<<<row_chunks, NORM_THREADS, 0, s>>>((const bf16*)dy, (const bf16*)x, rstd,
+                                                        gamma, (const bf16*)dadd, (bf16*)dx,
+                                                        dgamma_partials, rows, d);
+    colsum_pass2<<<(d + 255) / 256, 256, 0, s>>>(dgamma_partials, row_chunks, d, dgamma);
+    return cudaGetLastError();
+  }
   if (t == DT_F32)
     rmsnorm_bwd_kernel<float><<<row_chunks, NORM_THREADS, 0, s>>>(
         (const float*)dy, (const float*)x, rstd, gamma, (const float*)dadd, (float*)dx,

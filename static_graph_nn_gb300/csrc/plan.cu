@@ -36,6 +36,7 @@ constexpr size_t kAlignElems = 64;      // parameter offsets (256 B in fp32)
 constexpr size_t kWsAlign = 1024;       // workspace region alignment
 constexpr int kChunk = 16384;           // optimizer chunk (elements)
 constexpr int kRowChunks = 64;          // column-sum partial rows
+constexpr int kNormChunks = 4 * 152;    // RMSNorm backward blocks (dgamma partial rows)
 constexpr int kMsePartials = 1024;
 
 enum NodeKind { NK_LINEAR, NK_RMSNORM, NK_ATTN };
@@ -198,6 +199,8 @@ double gemm_bytes(const GemmArgs& g) {
   return b;
 }
 
+int norm_chunks(const mg_plan* p) { return p->batch < kNormChunks ? p->batch : kNormChunks; }
+
 bool tc_path(const mg_plan* p, const GemmArgs& g) { return p->use_tc && gemm_tc_eligible(g); }
 
 // error word of the tensor-core pipeline: 4 bytes after the loss scalar
@@ -338,7 +341,7 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
       site(e, nm, 0, bytes, 2, [&] {
         return rmsnorm_bwd(dt, gy, val_ptr(p, n.in, x), wsp<float>(p, n.rstd_off),
                            params + n.g_off, dx ? dadd : nullptr, dx,
-                           wsp<float>(p, p->partial_off), kRowChunks, grads + n.g_off,
+                           wsp<float>(p, p->partial_off), norm_chunks(p), grads + n.g_off,
                            p->batch, n.d, e.s);
       });
     } else {
@@ -599,6 +602,8 @@ void layout_workspace(mg_plan* p) {
   size_t maxw = 0;
   for (auto& v : p->values) maxw = v.width > (int)maxw ? v.width : maxw;
   size_t part = (size_t)kRowChunks * maxw * 4;
+  for (auto& n : p->nodes)
+    if (n.kind == NK_RMSNORM && (size_t)kNormChunks * n.d * 4 > part) part = (size_t)kNormChunks * n.d * 4;
   if (part < (size_t)kMsePartials * 4) part = (size_t)kMsePartials * 4;
   p->partial_off = b.take(part);
   p->ws_bytes = round_up(b.top, kWsAlign);
