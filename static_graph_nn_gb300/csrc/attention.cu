@@ -213,6 +213,14 @@ __global__ void __launch_bounds__(THREADS) attn_bwd_dkdv_kernel(const bf16* qkv,
 
 int attn_bwd_launches() { return 3; }
 
+cudaError_t attn_bwd_pre(const void* o, const void* dout, float* dsum, int nb, int S, int H,
+                         cudaStream_t s) {
+  int total = nb * S * H;
+  attn_bwd_pre_kernel<<<(total + 255) / 256, 256, 0, s>>>((const bf16*)o, (const bf16*)dout, dsum,
+                                                          nb, S, H);
+  return cudaGetLastError();
+}
+
 cudaError_t attn_fwd(const void* qkv, void* o, float* lse, int nb, int S, int H, int Dh,
                      cudaStream_t s) {
   if (Dh != DH || S % ROWS != 0) return cudaErrorInvalidValue;

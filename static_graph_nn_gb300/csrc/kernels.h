@@ -67,6 +67,17 @@ cudaError_t attn_fwd(const void* qkv, void* o, float* lse, int nb, int S, int H,
 cudaError_t attn_bwd(const void* qkv, const void* o, const void* dout, const float* lse,
                      float* dsum, void* dqkv, int nb, int S, int H, int Dh, cudaStream_t s);
 int attn_bwd_launches();
+// D_i = sum_c dO_ic O_ic into dsum [nb, H, S].
+cudaError_t attn_bwd_pre(const void* o, const void* dout, float* dsum, int nb, int S, int H,
+                         cudaStream_t s);
+// tcgen05 versions (head_dim 64, S a multiple of 128, 16-byte aligned rows).
+// *err is set to 1 if a bounded pipeline wait expires.
+bool attn_tc_eligible(int S, int H, int Dh, const void* qkv);
+cudaError_t attn_fwd_tc_launch(const void* qkv, void* o, float* lse, int nb, int S, int H,
+                               int* err, cudaStream_t s);
+cudaError_t attn_bwd_tc_launch(const void* qkv, const void* dout, const float* lse,
+                               const float* dsum, void* dqkv, int nb, int S, int H, int* err,
+                               cudaStream_t s);
 
 // ---- optimizer (multi-tensor over chunk tables) -----------------------------
 struct Chunk {  // a run of one tensor's elements in the flat buffers

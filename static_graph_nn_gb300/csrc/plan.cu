@@ -253,10 +253,16 @@ void forward_pass(Exec& e, const float* params, const void* x) {
       double flops = 4.0 * nb * n.nh * pairs * n.dh;
       double bytes = 2.0 * p->batch * 4.0 * n.nh * n.dh + 4.0 * nb * n.nh * n.S;
       char nm[96];
-      snprintf(nm, sizeof nm, "attn_fwd[l%d] b%d s%d h%d d%d", n.layer, nb, n.S, n.nh, n.dh);
+      const void* qkv = val_ptr(p, n.in, x);
+      const bool tc = p->use_tc && attn_tc_eligible(n.S, n.nh, n.dh, qkv);
+      snprintf(nm, sizeof nm, "attn_fwd[l%d] b%d s%d h%d d%d %s", n.layer, nb, n.S, n.nh, n.dh,
+               tc ? "tcgen05" : "simt");
       site(e, nm, flops, bytes, 1, [&] {
-        return attn_fwd(val_ptr(p, n.in, x), p->ws + p->values[n.out].off,
-                        wsp<float>(p, n.lse_off), nb, n.S, n.nh, n.dh, e.s);
+        if (tc)
+          return attn_fwd_tc_launch(qkv, p->ws + p->values[n.out].off, wsp<float>(p, n.lse_off),
+                                    nb, n.S, n.nh, err_word(p), e.s);
+        return attn_fwd(qkv, p->ws + p->values[n.out].off, wsp<float>(p, n.lse_off), nb, n.S,
+                        n.nh, n.dh, e.s);
       });
     }
   }
@@ -351,11 +357,20 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
       double flops = 10.0 * nb * n.nh * pairs * n.dh;
       double bytes = 2.0 * p->batch * n.nh * n.dh * (3 + 2 + 3);
       char nm[96];
-      snprintf(nm, sizeof nm, "attn_bwd[l%d] b%d s%d h%d d%d", n.layer, nb, n.S, n.nh, n.dh);
+      const void* qkv = val_ptr(p, n.in, x);
+      const bool tc = p->use_tc && attn_tc_eligible(n.S, n.nh, n.dh, qkv);
+      snprintf(nm, sizeof nm, "attn_bwd[l%d] b%d s%d h%d d%d %s", n.layer, nb, n.S, n.nh, n.dh,
+               tc ? "tcgen05" : "simt");
       site(e, nm, flops, bytes, attn_bwd_launches(), [&] {
-        return attn_bwd(val_ptr(p, n.in, x), p->ws + p->values[n.out].off, gy,
-                        wsp<float>(p, n.lse_off), wsp<float>(p, n.dsum_off), grad_ptr(p, n.in), nb,
-                        n.S, n.nh, n.dh, e.s);
+        if (tc) {
+          cudaError_t r = attn_bwd_pre(p->ws + p->values[n.out].off, gy, wsp<float>(p, n.dsum_off),
+                                       nb, n.S, n.nh, e.s);
+          if (r != cudaSuccess) return r;
+          return attn_bwd_tc_launch(qkv, gy, wsp<float>(p, n.lse_off), wsp<float>(p, n.dsum_off),
+                                    grad_ptr(p, n.in), nb, n.S, n.nh, err_word(p), e.s);
+        }
+        return attn_bwd(qkv, p->ws + p->values[n.out].off, gy, wsp<float>(p, n.lse_off),
+                        wsp<float>(p, n.dsum_off), grad_ptr(p, n.in), nb, n.S, n.nh, n.dh, e.s);
       });
     }
   }
