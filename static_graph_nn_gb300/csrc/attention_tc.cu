@@ -8,11 +8,13 @@
 // D_i = sum_c dO_ic O_ic:  P = exp(S - LSE), dP = dO V^T, dS = P (dP - D),
 // dV = P^T dO, dK = dS^T Q / 8, dQ = dS K / 8.
 //
-// Every kernel: one CTA per (128-row block, head, sequence), 160 threads.
-// Warp 0 lane 0 issues TMA loads and tcgen05.mma; warps 1-4 own one TMEM lane
-// (one row of the 128-row block) per thread, read S / dP with tcgen05.ld, do
-// the softmax arithmetic in fp32 and write bf16 P / dS tiles into shared
-// memory in the 128-byte-swizzled K-major layout the next MMA reads.
+// Every kernel: one CTA per (128-row block, head, sequence), 288 threads.
+// Warp 0 lane 0 issues TMA loads and tcgen05.mma; warps 1-8 each own one TMEM
+// lane quarter (32 rows of the 128-row block) and one half of the 128 columns,
+// read S / dP with tcgen05.ld, do the softmax arithmetic in fp32 and write bf16
+// P / dS tiles into shared memory in the 128-byte-swizzled K-major layout the
+// next MMA reads.  The two warps that share a row exchange its maximum through
+// shared memory (forward only).
 //   forward: S = Q K_j^T (TMEM) -> P (smem) -> O_j = P V_j (TMEM, two slots);
 //            O, the running max and sum stay in registers (online softmax).
 //   dK/dV:   per key block, over the query blocks that see it:
@@ -36,7 +38,9 @@ constexpr int AD = 64;                      // head dimension
 constexpr int AB = 128;                     // rows (queries / keys) per block
 constexpr uint32_t TILE = AB * AD * 2;      // one [128][64] bf16 tile: 16 KB
 constexpr uint32_t PTILE = 2 * TILE;        // one [128][128] bf16 tile: 32 KB (two K atoms)
-constexpr int AT_THREADS = 160;
+constexpr int NSW = 8;                      // softmax / elementwise warps (two per TMEM lane quarter)
+constexpr int AT_THREADS = 32 * (1 + NSW);
+constexpr int NSWT = 32 * NSW;              // their thread count
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct AttnArgs {
@@ -94,6 +98,11 @@ __device__ __forceinline__ void store8_bf16_row(bf16* out, const float* v, float
   }
 }
 
+// Barrier among the softmax / elementwise warps only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
 constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
 
@@ -128,6 +137,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
            *s_free = bar + 6, *p_full = bar + 7, *o_full = bar + 8, *o_free = bar + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red_max = reinterpret_cast<float*>(bar + 16);    // [2 iterations][2 halves][128]
+  float* red_l = red_max + 4 * AB;                        // [2 halves][128]
 
   const int nqb = A.S / AB;
   const int qb = nqb - 1 - blockIdx.x;             // longest rows of work first
@@ -143,11 +154,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 128);
+      mbar_init(&o_free[i], NSWT);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(p_full, 128);
+    mbar_init(s_free, NSWT);
+    mbar_init(p_full, NSWT);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -203,50 +214,64 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 1) >> 2;            // columns half*64 .. half*64+63
     const int r = quarter * 32 + lane;
     const int qi = qb * AB + r;                  // query position in the sequence
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float scale2 = LOG2E * 0.125f;         // log2(e) / sqrt(64)
-    float o[AD];
+    float o[32];                                 // O columns half*32 .. half*32+31
 #pragma unroll
-    for (int c = 0; c < AD; ++c) o[c] = 0.0f;
+    for (int c = 0; c < 32; ++c) o[c] = 0.0f;
     float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
     bool ok = true;
+    // Every thread passes the same named barriers, also after a failed wait,
+    // so that a timeout never leaves the other warps blocked at a barrier.
     for (int j = 0; j < nkb; ++j) {
-      if (!mbar_wait(s_full, j & 1)) { ok = false; break; }
-      tc_fence_after();
+      ok = ok && mbar_wait(s_full, j & 1);
+      const bool diag = (j == qb);
       float v[32];
       float mx = -INFINITY;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        tmem_ld32(tS + lane_off + c4 * 32, v);
+        for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
+          tmem_ld32(tS + lane_off + c4 * 32, v);
+          if (diag) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (j * AB + c4 * 32 + t <= qi) mx = fmaxf(mx, v[t]);
+            for (int t = 0; t < 32; ++t)
+              if (c4 * 32 + t <= r) mx = fmaxf(mx, v[t]);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) mx = fmaxf(mx, v[t]);
+          }
+        }
       }
+      float* rm = red_max + (j & 1) * 2 * AB;
+      rm[half * AB + r] = mx;
+      named_sync(1, NSWT);
+      if (!ok) continue;
+      mx = fmaxf(rm[r], rm[AB + r]);
       const float m_new = fmaxf(m, mx * scale2);
       const float alpha = exp2f(m - m_new);
       if (j > 0) {   // fold in O_{j-1}; its MMA has also finished reading P
-        if (!mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+        ok = mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (!ok) continue;
         tc_fence_after();
+        tmem_ld32(tO0 + ((j - 1) & 1) * 64 + half * 32 + lane_off, v);
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          tmem_ld32(tO0 + ((j - 1) & 1) * 64 + lane_off + c2 * 32, v);
-#pragma unroll
-          for (int t = 0; t < 32; ++t) o[c2 * 32 + t] = o[c2 * 32 + t] * alpha_prev + v[t];
-        }
+        for (int t = 0; t < 32; ++t) o[t] = o[t] * alpha_prev + v[t];
         tc_fence_before();
         mbar_arrive(&o_free[(j - 1) & 1]);
       }
       float lsum = 0.0f;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
         tmem_ld32(tS + lane_off + c4 * 32, v);
         float p[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          float e = (j * AB + c4 * 32 + t <= qi) ? exp2f(v[t] * scale2 - m_new) : 0.0f;
-          e = __bfloat162float(__float2bfloat16_rn(e));   // the value the MMA multiplies
+          float e = exp2f(v[t] * scale2 - m_new);
+          if (diag && c4 * 32 + t > r) e = 0.0f;
           p[t] = e;
           lsum += e;
         }
@@ -260,29 +285,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       m = m_new;
       alpha_prev = alpha;
     }
-    if (ok && mbar_wait(&o_full[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1)) {
+    ok = ok && mbar_wait(&o_full[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1);
+    if (ok) {
       tc_fence_after();
       float v[32];
+      tmem_ld32(tO0 + ((nkb - 1) & 1) * 64 + half * 32 + lane_off, v);
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        tmem_ld32(tO0 + ((nkb - 1) & 1) * 64 + lane_off + c2 * 32, v);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[c2 * 32 + t] = o[c2 * 32 + t] * alpha_prev + v[t];
-      }
-      const float inv = 1.0f / l;
-      bf16* orow = A.o + (size_t)(row0 + qi) * d + h * AD;
-#pragma unroll
-      for (int q = 0; q < AD / 8; ++q) {
-        uint4 u;
-        uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 hv = __floats2bfloat162_rn(o[q * 8 + 2 * i] * inv, o[q * 8 + 2 * i + 1] * inv);
-          w[i] = *reinterpret_cast<uint32_t*>(&hv);
-        }
-        reinterpret_cast<uint4*>(orow)[q] = u;
-      }
-      A.lse[((size_t)b * A.H + h) * A.S + qi] = (m + log2f(l)) / LOG2E;
+      for (int t = 0; t < 32; ++t) o[t] = o[t] * alpha_prev + v[t];
+    }
+    red_l[half * AB + r] = l;
+    named_sync(1, NSWT);
+    if (ok) {
+      const float lt = red_l[r] + red_l[AB + r];
+      const float inv = 1.0f / lt;
+      store8_bf16_row(A.o + (size_t)(row0 + qi) * d + h * AD + half * 32, o, inv);
+      if (half == 0) A.lse[((size_t)b * A.H + h) * A.S + qi] = (m + log2f(lt)) / LOG2E;
     } else {
       fail_wait(A.err, abort_flag);
     }
@@ -332,8 +349,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&in_empty[i], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(st_free, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(st_free, NSWT);
+    mbar_init(ds_full, NSWT);
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -399,32 +416,41 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 1) >> 2;            // query columns half*64 .. +63
     const int r = quarter * 32 + lane;
     const int kj = jb * AB + r;                  // key position
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float scale2 = LOG2E * 0.125f;
     bool ok = true;
     for (int t = 0; t < n_it; ++t) {
-      const int i = jb + t, bf = t & 1;
+      const int bf = t & 1;
       if (!mbar_wait(st_full, t & 1) || !mbar_wait(&in_full[bf], (t >> 1) & 1) ||
           (t > 0 && !mbar_wait(acc_done, (t - 1) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const bool diag = (t == 0);                // query block jb holds the diagonal
       const float* L = sL + bf * AB;
       const float* Dv = sD + bf * AB;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
         float s[32], dp[32];
         tmem_ld32(tSt + lane_off + c4 * 32, s);
         tmem_ld32(tdPt + lane_off + c4 * 32, dp);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int q = c4 * 32 + e;
-          float p = (i * AB + q >= kj) ? exp2f(s[e] * scale2 - L[q] * LOG2E) : 0.0f;
-          s[e] = p;
-          dp[e] = p * (dp[e] - Dv[q]);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = reinterpret_cast<const float4*>(L + c4 * 32)[e4];
+          const float4 d4 = reinterpret_cast<const float4*>(Dv + c4 * 32)[e4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e4 * 4 + u;
+            float p = exp2f(s[e] * scale2 - lv[u] * LOG2E);
+            if (diag && c4 * 32 + e < r) p = 0.0f;     // query < key
+            s[e] = p;
+            dp[e] = p * (dp[e] - dv[u]);
+          }
         }
         store_row_chunk(sPt, r, c4 * 4, s);
         store_row_chunk(sdSt, r, c4 * 4, dp);
@@ -436,16 +462,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     if (ok && mbar_wait(acc_done, (n_it - 1) & 1)) {
       tc_fence_after();
-      bf16* outk = A.dqkv + (size_t)(row0 + kj) * 3 * d + d + h * AD;
-      bf16* outv = A.dqkv + (size_t)(row0 + kj) * 3 * d + 2 * d + h * AD;
+      bf16* outk = A.dqkv + (size_t)(row0 + kj) * 3 * d + d + h * AD + half * 32;
+      bf16* outv = A.dqkv + (size_t)(row0 + kj) * 3 * d + 2 * d + h * AD + half * 32;
       float v[32];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        tmem_ld32(tdV + lane_off + c2 * 32, v);
-        store8_bf16_row(outv + c2 * 32, v, 1.0f);
-        tmem_ld32(tdK + lane_off + c2 * 32, v);
-        store8_bf16_row(outk + c2 * 32, v, 0.125f);
-      }
+      tmem_ld32(tdV + lane_off + half * 32, v);
+      store8_bf16_row(outv, v, 1.0f);
+      tmem_ld32(tdK + lane_off + half * 32, v);
+      store8_bf16_row(outk, v, 0.125f);
     } else {
       fail_wait(A.err, abort_flag);
     }
@@ -492,8 +515,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(s_free, NSWT);
+    mbar_init(ds_full, NSWT);
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -554,6 +577,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 1) >> 2;            // key columns half*64 .. +63
     const int r = quarter * 32 + lane;
     const int qi = ib * AB + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -567,14 +591,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         break;
       }
       tc_fence_after();
+      const bool diag = (t == ib);
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
         float s[32], dp[32];
         tmem_ld32(tS + lane_off + c4 * 32, s);
         tmem_ld32(tdP + lane_off + c4 * 32, dp);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p = (t * AB + c4 * 32 + e <= qi) ? exp2f(s[e] * scale2 - L2) : 0.0f;
+          float p = exp2f(s[e] * scale2 - L2);
+          if (diag && c4 * 32 + e > r) p = 0.0f;      // key > query
           dp[e] = p * (dp[e] - Di);
         }
         store_row_chunk(sdS, r, c4 * 4, dp);
@@ -586,13 +612,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     if (ok && mbar_wait(acc_done, (n_it - 1) & 1)) {
       tc_fence_after();
-      bf16* outq = A.dqkv + (size_t)(row0 + qi) * 3 * d + h * AD;
       float v[32];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        tmem_ld32(tdQ + lane_off + c2 * 32, v);
-        store8_bf16_row(outq + c2 * 32, v, 0.125f);
-      }
+      tmem_ld32(tdQ + lane_off + half * 32, v);
+      store8_bf16_row(A.dqkv + (size_t)(row0 + qi) * 3 * d + h * AD + half * 32, v, 0.125f);
     } else {
       fail_wait(A.err, abort_flag);
     }
@@ -638,7 +660,7 @@ bool map_128x64(CUtensorMap* m, const void* base, long long rows, long long cols
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t SMEM_FWD = 1024 + TILE * 5 + PTILE + 128;
+constexpr size_t SMEM_FWD = 1024 + TILE * 5 + PTILE + 128 + 6 * AB * 4;
 constexpr size_t SMEM_DKDV = 1024 + TILE * 6 + 2 * PTILE + 4 * AB * 4 + 128;
 constexpr size_t SMEM_DQ = 1024 + TILE * 6 + PTILE + 128;
 

@@ -265,6 +265,40 @@ cudaError_t launch_warp(const GemmArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Weight gradients with few output columns (dW = X^T dZ, A M-major, B
+// N-major, N <= 32): lanes take 32 consecutive rows m (coalesced A reads), the
+// 8 warps of a block split K, and the block adds its warps' partial sums.
+template <typename T, typename TO, typename TX>
+__global__ void __launch_bounds__(256) gemm_dw_narrow_kernel(const GemmArgs g) {
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int m = blockIdx.x * 32 + lane, n = blockIdx.y;
+  const T* A = static_cast<const T*>(g.A);
+  const T* B = static_cast<const T*>(g.B);
+  const int per = (g.K + 7) / 8;
+  const int k0 = w * per, k1 = min(g.K, k0 + per);
+  float acc = 0.0f;
+  if (m < g.M) {
+#pragma unroll 8
+    for (int k = k0; k < k1; ++k)
+      acc = fmaf(ld_elem(A, (size_t)k * g.lda + m), ld_elem(B, (size_t)k * g.ldb + n), acc);
+  }
+  red[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && m < g.M) {
+    float v = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v += red[i][lane];
+    epilogue_elem<TO, TX>(g, g.bias, m, n, v);
+  }
+}
+
+template <typename T, typename TO, typename TX>
+cudaError_t launch_dw_narrow(const GemmArgs& g, cudaStream_t s) {
+  gemm_dw_narrow_kernel<T, TO, TX><<<dim3((g.M + 31) / 32, g.N), 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
 template <typename T, typename TO, typename TX, bool A_MN, bool B_K, bool COMP = false>
 cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
@@ -278,6 +312,11 @@ cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
 // B K-major), dW (A M-major, B N-major, fp32 output).
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if (g.a_mn && !g.b_k && g.N <= 32 && g.out_type == DT_F32 && !g.act && !g.dact && !g.resid &&
+      !g.out_z) {   // narrow weight gradient
+    if (g.in_type == DT_F32) return launch_dw_narrow<float, float, float>(g, s);
+    return launch_dw_narrow<bf16, float, bf16>(g, s);
+  }
   if ((long long)g.M * g.N <= 65536 && g.K >= 64) {   // too few tiles: warp per output
     if (g.in_type == DT_F32) {
       if (!g.a_mn && !g.b_k) return launch_warp<float, float, float, true>(g, s);
