@@ -123,6 +123,23 @@ __device__ __forceinline__ void store_row_chunk(uint8_t* ptile, int r, int cc0, 
   }
 }
 
+// Same, from fp32 values kept as raw bits (computed in place in the TMEM load registers).
+__device__ __forceinline__ void store_row_chunk_bits(uint8_t* ptile, int r, int cc0, const uint32_t* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int cc = cc0 + q;
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * i]),
+                                                __uint_as_float(v[q * 8 + 2 * i + 1]));
+      w[i] = *reinterpret_cast<uint32_t*>(&hv);
+    }
+    *reinterpret_cast<uint4*>(ptile + (cc >> 3) * TILE + sw128(r, cc & 7)) = u;
+  }
+}
+
 // ============================================================ forward
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs A) {
@@ -229,21 +246,26 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     for (int j = 0; j < nkb; ++j) {
       ok = ok && mbar_wait(s_full, j & 1);
       const bool diag = (j == qb);
-      float v[32];
+      uint32_t sr[2][32];
       float mx = -INFINITY;
       if (ok) {
         tc_fence_after();
-#pragma unroll 1
-        for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
-          tmem_ld32(tS + lane_off + c4 * 32, v);
-          if (diag) {
+        tmem_ld32_async(tS + lane_off + half * 64, sr[0]);
+        tmem_ld32_async(tS + lane_off + half * 64 + 32, sr[1]);
+        tmem_wait();
+        tc_fence_before();
+        mbar_arrive(s_free);                       // S is in registers: the next QK^T may start
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-              if (c4 * 32 + t <= r) mx = fmaxf(mx, v[t]);
-          } else {
+              if (half * 64 + c * 32 + t <= r) mx = fmaxf(mx, __uint_as_float(sr[c][t]));
+        } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) mx = fmaxf(mx, v[t]);
-          }
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(sr[c][t]));
         }
       }
       float* rm = red_max + (j & 1) * 2 * AB;
@@ -257,6 +279,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         ok = mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
         if (!ok) continue;
         tc_fence_after();
+        float v[32];
         tmem_ld32(tO0 + ((j - 1) & 1) * 64 + half * 32 + lane_off, v);
 #pragma unroll
         for (int t = 0; t < 32; ++t) o[t] = o[t] * alpha_prev + v[t];
@@ -264,21 +287,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_arrive(&o_free[(j - 1) & 1]);
       }
       float lsum = 0.0f;
-#pragma unroll 1
-      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
-        tmem_ld32(tS + lane_off + c4 * 32, v);
-        float p[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          float e = exp2f(v[t] * scale2 - m_new);
-          if (diag && c4 * 32 + t > r) e = 0.0f;
-          p[t] = e;
+          float e = exp2f(__uint_as_float(sr[c][t]) * scale2 - m_new);
+          if (diag && half * 64 + c * 32 + t > r) e = 0.0f;
+          sr[c][t] = __float_as_uint(e);
           lsum += e;
         }
-        store_row_chunk(sP, r, c4 * 4, p);
+        store_row_chunk_bits(sP, r, (half * 2 + c) * 4, sr[c]);
       }
-      tc_fence_before();
-      mbar_arrive(s_free);
       fence_proxy_async();
       mbar_arrive(p_full);
       l = l * alpha + lsum;
@@ -586,27 +605,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const float Di = A.dsum[lrow + qi];
     bool ok = true;
     for (int t = 0; t < n_it; ++t) {
-      if (!mbar_wait(s_full, t & 1) || (t > 0 && !mbar_wait(acc_done, (t - 1) & 1))) {
+      if (!mbar_wait(s_full, t & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32_async(tS + lane_off + half * 64, sr[0]);
+      tmem_ld32_async(tS + lane_off + half * 64 + 32, sr[1]);
+      tmem_ld32_async(tdP + lane_off + half * 64, dr[0]);
+      tmem_ld32_async(tdP + lane_off + half * 64 + 32, dr[1]);
+      tmem_wait();
+      tc_fence_before();
+      mbar_arrive(s_free);                         // S, dP are in registers
+      if (t > 0 && !mbar_wait(acc_done, (t - 1) & 1)) {   // dS tile free again
+        ok = false;
+        break;
+      }
       const bool diag = (t == ib);
-#pragma unroll 1
-      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
-        float s[32], dp[32];
-        tmem_ld32(tS + lane_off + c4 * 32, s);
-        tmem_ld32(tdP + lane_off + c4 * 32, dp);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int c4 = half * 2 + c;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float p = exp2f(s[e] * scale2 - L2);
+          float p = exp2f(__uint_as_float(sr[c][e]) * scale2 - L2);
           if (diag && c4 * 32 + e > r) p = 0.0f;      // key > query
-          dp[e] = p * (dp[e] - Di);
+          dr[c][e] = __float_as_uint(p * (__uint_as_float(dr[c][e]) - Di));
         }
-        store_row_chunk(sdS, r, c4 * 4, dp);
+        store_row_chunk_bits(sdS, r, c4 * 4, dr[c]);
       }
-      tc_fence_before();
-      mbar_arrive(s_free);
       fence_proxy_async();
       mbar_arrive(ds_full);
     }
