@@ -36,6 +36,10 @@ cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
 // *err is set to 1 if a bounded pipeline wait expires.
 bool gemm_tc_eligible(const GemmArgs& g);
 cudaError_t gemm_tc(const GemmArgs& g, int* err, cudaStream_t s);
+// Same on a pair of SMs (tcgen05 cta_group::2, 256x256 tiles); requires
+// gemm_tc_eligible(g) as well.
+bool gemm_pair_eligible(const GemmArgs& g);
+cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s);
 
 // ---- loss ------------------------------------------------------------------
 // Softmax cross-entropy over rows of logits[B, C] (stride ld).  label_kind 0:

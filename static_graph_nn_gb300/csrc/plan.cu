@@ -103,6 +103,7 @@ struct mg_plan {
   int n_chunks = 0;
   const float* last_params = nullptr;
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
+  bool use_pair = true;      // SM-pair GEMMs for large shapes (MG_GEMM=tc1 turns them off)
   // schedule bookkeeping
   std::vector<Site> sites;
   int last_launches = 0;
@@ -206,14 +207,22 @@ bool tc_path(const mg_plan* p, const GemmArgs& g) { return p->use_tc && gemm_tc_
 // error word of the tensor-core pipeline: 4 bytes after the loss scalar
 int* err_word(mg_plan* p) { return reinterpret_cast<int*>(p->ws + p->loss_off + 4); }
 
+bool pair_path(const mg_plan* p, const GemmArgs& g) {
+  return p->use_pair && tc_path(p, g) && gemm_pair_eligible(g);
+}
+
 cudaError_t run_gemm(mg_plan* p, const GemmArgs& g, cudaStream_t s) {
+  if (pair_path(p, g)) return gemm_pair(g, err_word(p), s);
   if (tc_path(p, g)) return gemm_tc(g, err_word(p), s);
   return gemm_simt(g, s);
 }
 
 std::string gemm_name(const mg_plan* p, const char* what, int layer, const GemmArgs& g) {
   char b[160];
-  const char* kind = g.in_type != DT_BF16 ? "f32-ffma" : (tc_path(p, g) ? "bf16-tcgen05" : "bf16-simt");
+  const char* kind = g.in_type != DT_BF16 ? "f32-ffma"
+                     : pair_path(p, g)    ? "bf16-tcgen05x2"
+                     : tc_path(p, g)      ? "bf16-tcgen05"
+                                          : "bf16-simt";
   snprintf(b, sizeof b, "%s[l%d] %dx%dx%d %s", what, layer, g.M, g.N, g.K, kind);
   return b;
 }
@@ -703,7 +712,10 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     delete p;
     return r;
   }
-  if (const char* ev = getenv("MG_GEMM")) p->use_tc = strcmp(ev, "simt") != 0;
+  if (const char* ev = getenv("MG_GEMM")) {
+    p->use_tc = strcmp(ev, "simt") != 0;
+    p->use_pair = p->use_tc && strcmp(ev, "tc1") != 0;
+  }
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
   if (e != cudaSuccess) {

@@ -45,6 +45,25 @@ static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
   return false;
 }
 
+// Polling wait with cluster-scope acquire, for barriers that receive arrivals
+// from the other CTA of a pair (remote arrives, multicast commits); bounded,
+// false on timeout.
+static __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < (1u << 28); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 static __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y) {
   asm volatile(
