@@ -8,14 +8,15 @@
 //   dX       dH = dZ W^T   A = dZ [M,K] K-major,   B = W  [N,K] K-major
 //   dW       dW = X^T dZ   A = X  [K,M] M-major,   B = dZ [K,N] N-major
 //
-// One persistent CTA per SM, 192 threads in three roles:
+// One persistent CTA per SM, 320 threads in three roles:
 //   warp 0      TMA producer: loads 128xBK tiles of A and BNxBK tiles of B into
 //               a ring of shared-memory stages (128-byte swizzle);
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16) from
 //               one elected lane; tcgen05.commit frees each stage and
 //               publishes each finished accumulator;
-//   warps 2-5   epilogue: tcgen05.ld of one accumulator row per thread, bias,
-//               activation, derivative mask, residual, store to global.
+//   warps 2-9   epilogue: tcgen05.ld of one accumulator row per thread (two
+//               warps per TMEM lane quarter, each taking half the columns),
+//               bias, activation, derivative mask, residual, store to global.
 // Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap
 // the main loop of tile i+1.  Every mbarrier wait is bounded; on expiry the
 // kernel records the failure in an error word and unwinds instead of hanging.
@@ -32,7 +33,7 @@ using namespace tc;
 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;              // 64 bf16 = 128 bytes = one swizzle row
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;          // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 struct TcParams {
   GemmArgs g;
   int tiles_m, tiles_n, k_blocks;
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 256);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -260,8 +261,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9) ----------------
     const int quarter = warp & 3;              // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;          // columns half*BN/2 .. (half+1)*BN/2-1
     const int row_in_tile = quarter * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int m = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         if (m < P.g.M && n0 + c * 32 < P.g.N) epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);

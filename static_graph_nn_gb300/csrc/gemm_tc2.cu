@@ -8,7 +8,7 @@
 // of A and only half (128 columns) of B; the pair's tensor cores exchange the
 // B halves, so each SM moves 8 KB in and 8 KB out per 128 cycles.
 //
-// Cluster of 2 CTAs, one per SM, 192 threads each:
+// Cluster of 2 CTAs, one per SM, 320 threads each:
 //   warp 0      (both CTAs) TMA producer for this CTA's A rows and B columns;
 //               both CTAs' loads complete on the leader's full barrier
 //               (cp.async.bulk.tensor .cta_group::2), whose expected byte
@@ -17,8 +17,9 @@
 //               both SMs), waits for both CTAs' stages and issues
 //               tcgen05.mma.cta_group::2 (M=256, N=256, K=16); its commits are
 //               multicast to both CTAs (stage free, accumulator full);
-//   warps 2-5   (both CTAs) epilogue on this CTA's 128 accumulator rows, then
-//               a remote arrive on the leader's accumulator-free barrier.
+//   warps 2-9   (both CTAs) epilogue on this CTA's 128 accumulator rows, two
+//               warps per TMEM lane quarter splitting the 256 columns, then a
+//               remote arrive on the leader's accumulator-free barrier.
 // Every wait is bounded; on expiry the error word is set and the pair unwinds.
 #include <cuda.h>
 
@@ -35,8 +36,8 @@ constexpr int P_BM = 128;          // rows per CTA (256 per pair)
 constexpr int P_BNH = 128;         // B columns per CTA (256 per pair)
 constexpr int P_BN = 256;
 constexpr int P_BK = 64;
-constexpr int P_STAGES = 6;
-constexpr int P_THREADS = 192;
+constexpr int P_STAGES = 7;
+constexpr int P_THREADS = 320;          // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t P_A_BYTES = P_BM * P_BK * 2;
 constexpr uint32_t P_B_BYTES = P_BNH * P_BK * 2;
 
@@ -231,7 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * 128);
+      mbar_init(&tempty[a], 2 * 256);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -314,8 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
-    const int quarter = warp & 3;
+    // ---------------- epilogue (warps 2..9, both CTAs) ----------------
+    const int quarter = warp & 3;                // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;            // columns half*128 .. half*128+127
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t leader_tempty[2] = {map_to(&tempty[0], 0), map_to(&tempty[1], 0)};
     int it = 0;
@@ -330,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const int m = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * P_BN);
 #pragma unroll 1
-      for (int c = 0; c < P_BN / 32; ++c) {
+      for (int c = half * (P_BN / 64); c < (half + 1) * (P_BN / 64); ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         if (m < P.g.M && n0 + c * 32 < P.g.N) epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
