@@ -26,6 +26,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# DRAM bytes per launch of the dominant kernel from one ncu capture of the
+# current code (profiles/), keyed by kernel family; None when not captured.
+TRAFFIC = {}
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (maximum SM clock)
 FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -156,6 +160,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(self.rows)}
 
 
+def kernel_family(site_name: str) -> str:
+    """The CUDA kernel a schedule entry launches, from its name."""
+    n = site_name
+    if n.startswith(("fwd[", "dX[", "dW[")):
+        if "tcgen05x2" in n:
+            return "gemm_pair_kernel (tcgen05 cta_group::2)"
+        if "tcgen05" in n:
+            return "gemm_tc_kernel (tcgen05)"
+        if "f32-ffma" in n:
+            return "gemm_simt (fp32 FFMA)"
+        return "gemm_simt (bf16)"
+    if n.startswith("attn_fwd"):
+        return "attn_fwd" + (" (tcgen05)" if "tcgen05" in n else " (simt)")
+    if n.startswith("attn_bwd"):
+        return "attn_bwd dq+dkdv" + (" (tcgen05)" if "tcgen05" in n else " (simt)")
+    return n.split("[")[0].split(" ")[0]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -264,6 +286,7 @@ def main():
     import __graft_entry__
     from static_graph_nn_gb300 import Plan
     from static_graph_nn_gb300 import workloads as W
+    from static_graph_nn_gb300.replicas import job_throughput, max_over_ranks
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -351,13 +374,7 @@ def main():
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
-    ms_t = torch.tensor([ms], device="cuda")
-    e2e_t = torch.tensor([e2e_s], device="cuda")
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
-    e2e_s = float(e2e_t.item())
+    ms, e2e_s = max_over_ranks([ms, e2e_s], device="cuda")
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -369,18 +386,27 @@ def main():
     bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
 
-    # dominant kernel (largest share of the timed region)
-    top = max(prof, key=lambda e: e["total_ms"])
-    avg_ms = top["total_ms"] / max(1, top["launches"])
+    # dominant kernel: schedule entries grouped by the kernel they launch (the
+    # view of the ncu launch list); achieved = algorithmic work per launch /
+    # average launch duration, i.e. the group's work / its time
+    fam = {}
+    for e in prof:
+        k = kernel_family(e["name"])
+        f = fam.setdefault(k, {"name": k, "launches": 0, "total_ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        f["launches"] += e["launches"]
+        f["total_ms"] += e["total_ms"]
+        f["flops"] += e["flops"] * e["launches"]
+        f["bytes"] += e["bytes"] * e["launches"]
+    top = max(fam.values(), key=lambda f: f["total_ms"])
     if top["flops"] > 0:
         if prec == "bf16":
             bound, unit, peak = "tensor", "TFLOP/s", bf16_peak
         else:
             bound, unit, peak = "alu", "TFLOP/s", FP32_FFMA_TFLOPS
-        achieved = top["flops"] / (avg_ms * 1e-3) / 1e12
+        achieved = top["flops"] / (top["total_ms"] * 1e-3) / 1e12
     else:
         bound, unit, peak = "hbm", "GB/s", hbm_peak
-        achieved = top["bytes"] / (avg_ms * 1e-3) / 1e9
+        achieved = top["bytes"] / (top["total_ms"] * 1e-3) / 1e9
     total_prof = sum(e["total_ms"] for e in prof)
     kernels = [{"name": e["name"], "share": e["total_ms"] / total_prof if total_prof else None,
                 "avg_ms": e["total_ms"] / max(1, e["launches"]),
@@ -390,7 +416,7 @@ def main():
                 if e["total_ms"] else None}
                for e in sorted(prof, key=lambda e: -e["total_ms"])[:8]]
 
-    value = world * 1e3 / ms_step
+    value = job_throughput(world, args.steps, ms * 1e-3)
     h2d = x_host.numel() * x_host.element_size() + y_host.numel() * y_host.element_size()
     line = {
         "metric": "training steps/s (achieved TFLOP/s per step)",
@@ -405,14 +431,21 @@ def main():
         "tflops": flops / (ms_step * 1e-3) / 1e12,
         "pct_of_peak": flops / (ms_step * 1e-3) / 1e12 / (bf16_peak if prec == "bf16" else FP32_FFMA_TFLOPS),
         "peak_source": peak_src,
-        "roofline": {"kernel": top["name"], "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": None,
+        "roofline": {"kernel": top["name"], "launches_timed": top["launches"],
+                     "share": top["total_ms"] / total_prof if total_prof else None,
+                     "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": unit, "frac": achieved / peak, "traffic": TRAFFIC.get(top["name"]),
                      "peak_note": f"{'sustained bf16' if bound == 'tensor' else bound} peak, {peak_src}"},
         "kernels": kernels,
+        "kernel_families": [{"kernel": f["name"], "launches": f["launches"],
+                             "share": f["total_ms"] / total_prof if total_prof else None,
+                             "tflops": f["flops"] / (f["total_ms"] * 1e-3) / 1e12 if f["flops"] and f["total_ms"] else None,
+                             "gbs": f["bytes"] / (f["total_ms"] * 1e-3) / 1e9 if f["total_ms"] else None}
+                            for f in sorted(fam.values(), key=lambda f: -f["total_ms"])],
         "gpu_launches": launches,
         "loss": loss,
         "clocks": clk,
-        "e2e": {"value": world / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, 1, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 4},
         "plan_workspace_bytes": plan.workspace_bytes,
     }

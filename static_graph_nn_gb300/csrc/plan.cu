@@ -68,6 +68,8 @@ struct Node {
   // attention
   int nh = 0, dh = 0, S = 0;
   size_t lse_off = 0, dsum_off = 0;
+  // parameter tensors of this node: t0 .. t0+nt-1
+  int t0 = 0, nt = 0;
 };
 
 struct Site {
@@ -106,6 +108,12 @@ struct mg_plan {
   bool use_pair = true;      // SM-pair GEMMs for large shapes (MG_GEMM=tc1 turns them off)
   // schedule bookkeeping
   std::vector<Site> sites;
+  // update of each node's parameters on a second stream, overlapping the rest
+  // of the backward pass (the optimizer is bandwidth-bound, the GEMMs are not)
+  cudaStream_t aux = nullptr;
+  std::vector<cudaEvent_t> node_ev;
+  cudaEvent_t join_ev = nullptr;
+  std::vector<int> tensor_chunk;     // first chunk of tensor t; [n_tensors] = n_chunks
   int last_launches = 0;
   bool profiling = false;
   int prof_max = 0, prof_calls = 0;
@@ -154,10 +162,27 @@ struct Exec {
   int cursor = 0;
   int launches = 0;
   cudaError_t err = cudaSuccess;
+  // optimizer arguments of a training step
+  float* params = nullptr;
+  float* grads = nullptr;
+  float* m = nullptr;
+  float* v = nullptr;
+  float lr = 0.f;
+  int step = 1;
 };
 
 template <class F>
+void site_on(Exec& e, cudaStream_t st, const std::string& name, double flops, double bytes,
+             int kernels, F&& f);
+
+template <class F>
 void site(Exec& e, const std::string& name, double flops, double bytes, int kernels, F&& f) {
+  site_on(e, e.s, name, flops, bytes, kernels, static_cast<F&&>(f));
+}
+
+template <class F>
+void site_on(Exec& e, cudaStream_t st, const std::string& name, double flops, double bytes,
+             int kernels, F&& f) {
   mg_plan* p = e.p;
   int id = e.cursor++;
   if (e.dry) {
@@ -172,10 +197,10 @@ void site(Exec& e, const std::string& name, double flops, double bytes, int kern
   if (e.err != cudaSuccess) return;
   const int ns = (int)p->sites.size();
   const bool rec = e.profile && p->profiling && p->prof_calls < p->prof_max && id < ns;
-  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2], e.s);
+  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2], st);
   cudaError_t r = f();
   if (r != cudaSuccess) e.err = r;
-  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2 + 1], e.s);
+  if (rec) cudaEventRecord(p->events[((size_t)p->prof_calls * ns + id) * 2 + 1], st);
   e.launches += kernels;
 }
 
@@ -302,6 +327,40 @@ void loss_pass(Exec& e, const void* labels) {
   }
 }
 
+// Optimizer update of node ni's parameters, on the auxiliary stream once the
+// node's backward kernels (the last readers of its weights) have run.
+void node_update(Exec& e, int ni) {
+  mg_plan* p = e.p;
+  const Node& n = p->nodes[ni];
+  if (n.nt == 0) return;
+  const int c0 = p->tensor_chunk[n.t0], c1 = p->tensor_chunk[n.t0 + n.nt];
+  double np = 0;
+  for (int t = n.t0; t < n.t0 + n.nt; ++t) np += (double)p->p_rows[t] * p->p_cols[t];
+  const Chunk* chunks = wsp<Chunk>(p, p->chunks_off) + c0;
+  void* shadow = p->dt == DT_BF16 ? p->ws + p->shadow_off : nullptr;
+  if (!e.dry && e.err == cudaSuccess) {
+    cudaError_t r = cudaEventRecord(p->node_ev[ni], e.s);
+    if (r == cudaSuccess) r = cudaStreamWaitEvent(p->aux, p->node_ev[ni], 0);
+    if (r != cudaSuccess) e.err = r;
+  }
+  char nm[96];
+  if (p->optimizer == MG_OPT_ADAM) {
+    double bc1 = 1.0 - std::pow((double)p->beta1, (double)e.step);
+    double bc2 = 1.0 - std::pow((double)p->beta2, (double)e.step);
+    float lr_bc1 = (float)(e.lr / bc1), inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    snprintf(nm, sizeof nm, "adam[l%d] %.0f params", n.layer, np);
+    site_on(e, p->aux, nm, 0, np * (28.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
+      return adam_update(chunks, c1 - c0, e.params, e.grads, e.m, e.v, shadow, lr_bc1,
+                         inv_sqrt_bc2, p->beta1, p->beta2, p->adam_eps, p->aux);
+    });
+  } else {
+    snprintf(nm, sizeof nm, "sgd[l%d] %.0f params", n.layer, np);
+    site_on(e, p->aux, nm, 0, np * (12.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
+      return sgd_update(chunks, c1 - c0, e.params, e.grads, shadow, e.lr, p->aux);
+    });
+  }
+}
+
 void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
   mg_plan* p = e.p;
   const DType dt = p->dt;
@@ -348,6 +407,7 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
         site(e, gemm_name(p, "dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
              [&] { return run_gemm(p, h, e.s); });
       }
+      node_update(e, ni);
     } else if (n.kind == NK_RMSNORM) {
       void* dx = vin.need_grad ? grad_ptr(p, n.in) : nullptr;
       double bytes = (double)dtype_size(dt) * p->batch * n.d * (dx ? (dadd ? 4 : 3) : 2);
@@ -359,6 +419,7 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
                            wsp<float>(p, p->partial_off), norm_chunks(p), grads + n.g_off,
                            p->batch, n.d, e.s);
       });
+      node_update(e, ni);
     } else {
       if (!vin.need_grad) continue;
       int nb = p->batch / n.S;
@@ -385,32 +446,28 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
   }
 }
 
-void optimizer_pass(Exec& e, float* params, float* grads, float* m, float* v, float lr, int step) {
+// The step ends when the auxiliary stream's updates have: the caller's stream
+// waits for them.
+void join_updates(Exec& e) {
   mg_plan* p = e.p;
-  const Chunk* chunks = wsp<Chunk>(p, p->chunks_off);
-  void* shadow = p->dt == DT_BF16 ? p->ws + p->shadow_off : nullptr;
-  double np = (double)p->n_params;
-  if (p->optimizer == MG_OPT_ADAM) {
-    double bc1 = 1.0 - std::pow((double)p->beta1, (double)step);
-    double bc2 = 1.0 - std::pow((double)p->beta2, (double)step);
-    float lr_bc1 = (float)(lr / bc1), inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
-    site(e, "adam_multi_tensor", 0, np * (28.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
-      return adam_update(chunks, p->n_chunks, params, grads, m, v, shadow, lr_bc1, inv_sqrt_bc2,
-                         p->beta1, p->beta2, p->adam_eps, e.s);
-    });
-  } else {
-    site(e, "sgd_multi_tensor", 0, np * (12.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
-      return sgd_update(chunks, p->n_chunks, params, grads, shadow, lr, e.s);
-    });
-  }
+  if (e.dry || e.err != cudaSuccess) return;
+  cudaError_t r = cudaEventRecord(p->join_ev, p->aux);
+  if (r == cudaSuccess) r = cudaStreamWaitEvent(e.s, p->join_ev, 0);
+  if (r != cudaSuccess) e.err = r;
 }
 
 void train_schedule(Exec& e, float* params, float* grads, float* m, float* v, const void* x,
                     const void* labels, float lr, int step) {
+  e.params = params;
+  e.grads = grads;
+  e.m = m;
+  e.v = v;
+  e.lr = lr;
+  e.step = step;
   forward_pass(e, params, x);
   loss_pass(e, labels);
   backward_pass(e, params, grads, x);
-  optimizer_pass(e, params, grads, m, v, lr, step);
+  join_updates(e);
 }
 
 // ---- descriptor compile ------------------------------------------------------
@@ -484,8 +541,10 @@ mg_status compile(mg_plan* p, const mg_graph_desc* d) {
         n.d_in = l.d_in;
         n.d_out = l.d_out;
         n.has_bias = l.has_bias ? 1 : 0;
+        n.t0 = (int)p->p_off.size();
         n.w_off = add_param(l.d_in, l.d_out, 1);
         if (n.has_bias) n.b_off = add_param(1, l.d_out, 0);
+        n.nt = (int)p->p_off.size() - n.t0;
         if (i + 1 < nl && (p->layers[i + 1].op == MG_OP_RELU || p->layers[i + 1].op == MG_OP_GELU_TANH)) {
           n.act = p->layers[i + 1].op == MG_OP_RELU ? ACT_RELU : ACT_GELU;
           ++i;
@@ -523,7 +582,9 @@ mg_status compile(mg_plan* p, const mg_graph_desc* d) {
         n.in = cur;
         n.d = l.d_in;
         n.eps = l.eps;
+        n.t0 = (int)p->p_off.size();
         n.g_off = add_param(1, l.d_in, 0);
+        n.nt = 1;
         int ni = (int)p->nodes.size();
         n.out = new_value(l.d_in, ni);
         p->values[n.in].consumers++;
@@ -633,9 +694,11 @@ void layout_workspace(mg_plan* p) {
   p->ws_bytes = round_up(b.top, kWsAlign);
 }
 
-std::vector<Chunk> chunk_table(const mg_plan* p) {
+std::vector<Chunk> chunk_table(mg_plan* p) {
   std::vector<Chunk> t;
+  p->tensor_chunk.assign(p->p_off.size() + 1, 0);
   for (size_t i = 0; i < p->p_off.size(); ++i) {
+    p->tensor_chunk[i] = (int)t.size();
     size_t len = (size_t)p->p_rows[i] * p->p_cols[i];
     for (size_t s = 0; s < len; s += kChunk) {
       Chunk c;
@@ -645,6 +708,7 @@ std::vector<Chunk> chunk_table(const mg_plan* p) {
       t.push_back(c);
     }
   }
+  p->tensor_chunk[p->p_off.size()] = (int)t.size();
   return t;
 }
 
@@ -728,8 +792,17 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
   std::vector<Chunk> ch = chunk_table(p);
   e = cudaMemcpy(p->ws + p->chunks_off, ch.data(), ch.size() * sizeof(Chunk), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->ws + p->loss_off, 0, 16);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking);
+  p->node_ev.assign(p->nodes.size(), nullptr);
+  for (auto& ev : p->node_ev)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     mg_status r = cuda_fail(nullptr, e, "workspace init");
+    for (auto ev : p->node_ev)
+      if (ev) cudaEventDestroy(ev);
+    if (p->join_ev) cudaEventDestroy(p->join_ev);
+    if (p->aux) cudaStreamDestroy(p->aux);
     cudaFree(p->ws);
     delete p;
     return r;
@@ -749,6 +822,10 @@ void mg_step_plan_destroy(mg_plan* p) {
   cudaSetDevice(p->device);
   cudaDeviceSynchronize();
   for (auto ev : p->events) cudaEventDestroy(ev);
+  for (auto ev : p->node_ev)
+    if (ev) cudaEventDestroy(ev);
+  if (p->join_ev) cudaEventDestroy(p->join_ev);
+  if (p->aux) cudaStreamDestroy(p->aux);
   if (p->ws) cudaFree(p->ws);
   if (prev >= 0) cudaSetDevice(prev);
   delete p;
