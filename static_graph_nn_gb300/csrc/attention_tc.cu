@@ -98,32 +98,25 @@ __device__ __forceinline__ void store8_bf16_row(bf16* out, const float* v, float
   }
 }
 
-// Barrier among the softmax / elementwise warps only (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void named_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// 2^x on the special-function unit, subnormal results flushed to zero (the
+// probabilities they stand for are far below bf16 resolution next to the
+// row maximum's 1); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
 constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
 constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
 
-// 32 fp32 values -> bf16, written as four 16-byte chunks of row r (column
-// chunks cc0..cc0+3 of a two-atom [128][128] tile).
-__device__ __forceinline__ void store_row_chunk(uint8_t* ptile, int r, int cc0, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int cc = cc0 + q;
-    uint4 u;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 hv = __floats2bfloat162_rn(v[q * 8 + 2 * i], v[q * 8 + 2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&hv);
-    }
-    *reinterpret_cast<uint4*>(ptile + (cc >> 3) * TILE + sw128(r, cc & 7)) = u;
-  }
-}
-
-// Same, from fp32 values kept as raw bits (computed in place in the TMEM load registers).
+// 32 fp32 values held as raw bits (computed in place in the TMEM load
+// registers) -> bf16, written as four 16-byte chunks of row r (column chunks
+// cc0..cc0+3 of a two-atom [128][128] tile).
 __device__ __forceinline__ void store_row_chunk_bits(uint8_t* ptile, int r, int cc0, const uint32_t* v) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -141,194 +134,316 @@ __device__ __forceinline__ void store_row_chunk_bits(uint8_t* ptile, int r, int 
 }
 
 // ============================================================ forward
-__global__ void __launch_bounds__(AT_THREADS, 1)
-    attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs A) {
+// Persistent, one CTA per SM.  A work unit is a pair of consecutive query
+// blocks (2p, 2p+1) of one (head, sequence).  Warps 0-3 own query block 2p
+// (tile 0) and warps 4-7 block 2p+1 (tile 1), one query row per thread; warp 8
+// is the TMA producer, warp 9 issues the MMAs.  Per key block j and tile w:
+//   S_w = Q_w K_j^T          TMEM, fp32, 128 columns
+//   P_w = 2^(S_w/8 log2e - m) TMEM, bf16 pairs, 64 columns
+//   O_w += P_w V_j           TMEM, fp32, 64 columns (A operand read from TMEM)
+// While one tile's softmax runs, the tensor core works on the other tile.
+// m is the row's reference maximum (log2 units); it is raised, and O and l
+// rescaled, only when a block's maximum exceeds it by more than 8, so that
+// P <= 2^8.  Tile 0 skips key block 2p+1, which lies after all its queries.
+// Units are dealt to the CTAs heaviest first in snake order.
+constexpr int FWD_THREADS = 320;
+constexpr int FWD_NST = 3;                            // K/V ring stages
+constexpr uint32_t F_S = 0, F_P = 256, F_O = 384;     // TMEM columns of S, P, O (tile 0)
+constexpr float RESCALE_T = 8.0f;
+
+struct FwdUnit {
+  int p, h, b, n0, n1;   // pair, head, sequence; key blocks of tile 0 / tile 1 (0: no tile 1)
+};
+
+__device__ __forceinline__ bool fwd_unit(int k, int n_units, int npair, int nqb, int H, FwdUnit& U) {
+  const int G = gridDim.x;
+  const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  if (u >= n_units) return false;
+  const int hb = n_units / npair;
+  U.p = npair - 1 - u / hb;
+  U.h = (u % hb) % H;
+  U.b = (u % hb) / H;
+  U.n0 = 2 * U.p + 1;
+  U.n1 = (2 * U.p + 1 < nqb) ? 2 * U.p + 2 : 0;
+  return true;
+}
+
+// 32 fp32 S values (raw bits) of row r at columns col0.. : keys after the
+// query get -inf when the block is the diagonal one.
+__device__ __forceinline__ void mask_diag(uint32_t (&v)[32], int col0, int r) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (col0 + e > r) v[e] = 0xff800000u;
+}
+
+__global__ void __launch_bounds__(FWD_THREADS, 1)
+    attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sQ = sm;
-  uint8_t* sK = sQ + TILE;           // [2]
-  uint8_t* sV = sK + 2 * TILE;       // [2]
-  uint8_t* sP = sV + 2 * TILE;       // 32 KB
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + PTILE);
-  uint64_t *q_full = bar, *kv_full = bar + 1, *kv_empty = bar + 3, *s_full = bar + 5,
-           *s_free = bar + 6, *p_full = bar + 7, *o_full = bar + 8, *o_free = bar + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
+  uint8_t* sQ = sm;                          // [2 slots][2 tiles]
+  uint8_t* sK = sQ + 4 * TILE;               // [FWD_NST]
+  uint8_t* sV = sK + FWD_NST * TILE;         // [FWD_NST]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sV + FWD_NST * TILE);
+  uint64_t *q_full = bar, *q_empty = bar + 2, *kv_full = bar + 4, *kv_empty = kv_full + FWD_NST;
+  uint64_t *s_full = kv_empty + FWD_NST, *p_full = s_full + 2, *o_done = s_full + 4,
+           *o_free = s_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red_max = reinterpret_cast<float*>(bar + 16);    // [2 iterations][2 halves][128]
-  float* red_l = red_max + 4 * AB;                        // [2 halves][128]
 
   const int nqb = A.S / AB;
-  const int qb = nqb - 1 - blockIdx.x;             // longest rows of work first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int nkb = qb + 1;
+  const int npair = (nqb + 1) / 2;
+  const int n_units = npair * A.H * nb;
   const int d = A.H * AD;
-  const int row0 = b * A.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], 128);
+    }
+    for (int i = 0; i < FWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], NSWT);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, NSWT);
-    mbar_init(p_full, NSWT);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  if (warp == 9) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = *tmem_slot;            // columns 0..127
-  const uint32_t tO0 = tS + 128;             // two 64-column slots
+  const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
-      auto load_kv = [&](int j) {
-        mbar_expect_tx(&kv_full[j & 1], 2 * TILE);
-        tma_load_2d(sK + (j & 1) * TILE, &tm_qkv, &kv_full[j & 1], d + h * AD, row0 + j * AB);
-        tma_load_2d(sV + (j & 1) * TILE, &tm_qkv, &kv_full[j & 1], 2 * d + h * AD, row0 + j * AB);
-      };
-      auto mma_pv = [&](int i) -> bool {
-        if (!mbar_wait(p_full, i & 1)) return false;
-        if (i >= 2 && !mbar_wait(&o_free[i & 1], ((i - 2) >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint8_t* v = sV + (i & 1) * TILE;
-#pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16(tO0 + (i & 1) * 64, kdesc_p(sP, kk), mndesc(v, kk), IDESC_128x64_KMN, kk > 0);
-        mma_commit(&o_full[i & 1]);
-        mma_commit(&kv_empty[i & 1]);
-        return true;
-      };
       bool ok = true;
-      mbar_expect_tx(q_full, TILE);
-      tma_load_2d(sQ, &tm_qkv, q_full, h * AD, row0 + qb * AB);
-      load_kv(0);
-      if (nkb > 1) load_kv(1);
-      for (int j = 0; j < nkb && ok; ++j) {
-        ok = mbar_wait(&kv_full[j & 1], (j >> 1) & 1) && (j > 0 || mbar_wait(q_full, 0)) &&
-             (j == 0 || mbar_wait(s_free, (j - 1) & 1));
+      int g = 0;
+      FwdUnit U;
+      for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
+        const int row0 = U.b * A.S, slot = k & 1;
+        const int nmax = U.n1 ? U.n1 : U.n0;
+        ok = mbar_wait(&q_empty[slot], ((k >> 1) & 1) ^ 1);
         if (!ok) break;
-        tc_fence_after();
-        const uint8_t* k = sK + (j & 1) * TILE;
-#pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_bf16(tS, kdesc(sQ, kk), kdesc(k, kk), IDESC_128x128_KK, kk > 0);
-        mma_commit(s_full);
-        if (j > 0) ok = mma_pv(j - 1);
-        if (ok && j + 1 < nkb && j + 1 >= 2) {
-          ok = mbar_wait(&kv_empty[(j + 1) & 1], ((j - 1) >> 1) & 1);
-          if (ok) load_kv(j + 1);
+        mbar_expect_tx(&q_full[slot], (U.n1 ? 2 : 1) * TILE);
+        tma_load_2d(sQ + (2 * slot) * TILE, &tm_qkv, &q_full[slot], U.h * AD, row0 + 2 * U.p * AB);
+        if (U.n1)
+          tma_load_2d(sQ + (2 * slot + 1) * TILE, &tm_qkv, &q_full[slot], U.h * AD,
+                      row0 + (2 * U.p + 1) * AB);
+        for (int j = 0; j < nmax; ++j, ++g) {
+          const int st = g % FWD_NST;
+          ok = mbar_wait(&kv_empty[st], ((g / FWD_NST) & 1) ^ 1);
+          if (!ok) break;
+          mbar_expect_tx(&kv_full[st], 2 * TILE);
+          tma_load_2d(sK + st * TILE, &tm_qkv, &kv_full[st], d + U.h * AD, row0 + j * AB);
+          tma_load_2d(sV + st * TILE, &tm_qkv, &kv_full[st], 2 * d + U.h * AD, row0 + j * AB);
         }
       }
-      if (ok) ok = mma_pv(nkb - 1);
+      if (!ok) fail_wait(A.err, abort_flag);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      int g = 0;
+      int c[2] = {0, 0};     // S/P iterations issued per tile
+      int uo[2] = {0, 0};    // units started per tile
+      // the previous step, whose P V products are still to be issued
+      int pv_st = -1, pv_act = 0, pv_first = 0;
+      auto issue_pv = [&](int w) -> bool {
+        // P_w of tile-iteration c[w]-1 is complete (this also frees S_w)
+        if (!mbar_wait(&p_full[w], (c[w] - 1) & 1)) return false;
+        if ((pv_first >> w) & 1) {
+          if (uo[w] > 1 && !mbar_wait(&o_free[w], (uo[w] - 2) & 1)) return false;
+        }
+        tc_fence_after();
+        const uint8_t* v = sV + pv_st * TILE;
+#pragma unroll
+        for (int kk = 0; kk < AB / 16; ++kk)
+          mma_bf16_ts(tbase + F_O + 64 * w, tbase + F_P + 64 * w + kk * 8, mndesc(v, kk),
+                      IDESC_128x64_KMN, !(((pv_first >> w) & 1) && kk == 0));
+        mma_commit(&o_done[w]);
+        return true;
+      };
+      FwdUnit U;
+      for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
+        const int slot = k & 1;
+        const int nmax = U.n1 ? U.n1 : U.n0;
+        ok = mbar_wait(&q_full[slot], (k >> 1) & 1);
+        for (int j = 0; ok && j < nmax; ++j, ++g) {
+          const int st = g % FWD_NST;
+          const int act = (j < U.n0 ? 1 : 0) | (j < U.n1 ? 2 : 0);
+          ok = mbar_wait(&kv_full[st], (g / FWD_NST) & 1);
+          if (!ok) break;
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            if ((pv_act >> w) & 1) {
+              ok = issue_pv(w);
+              if (!ok) break;
+            }
+            if ((act >> w) & 1) {
+              tc_fence_after();
+              const uint8_t* q = sQ + (2 * slot + w) * TILE;
+              const uint8_t* kt = sK + st * TILE;
+#pragma unroll
+              for (int kk = 0; kk < AD / 16; ++kk)
+                mma_bf16(tbase + F_S + 128 * w, kdesc(q, kk), kdesc(kt, kk), IDESC_128x128_KK, kk > 0);
+              mma_commit(&s_full[w]);
+              ++c[w];
+            }
+          }
+          if (!ok) break;
+          if (pv_act) mma_commit(&kv_empty[pv_st]);
+          if (j == nmax - 1) mma_commit(&q_empty[slot]);
+          if (j == 0) {   // counted after the previous unit's last P V products
+            if (U.n0) ++uo[0];
+            if (U.n1) ++uo[1];
+          }
+          pv_st = st;
+          pv_act = act;
+          pv_first = (j == 0) ? act : 0;
+        }
+      }
+      if (ok && pv_act) {
+        for (int w = 0; w < 2 && ok; ++w)
+          if ((pv_act >> w) & 1) ok = issue_pv(w);
+        if (ok) mma_commit(&kv_empty[pv_st]);
+      }
       if (!ok) fail_wait(A.err, abort_flag);
     }
   } else {
+    // ---------------- softmax: warps 0-3 tile 0, warps 4-7 tile 1 ----------------
+    const int w = warp >> 2;
     const int quarter = warp & 3;
-    const int half = (warp - 1) >> 2;            // columns half*64 .. half*64+63
     const int r = quarter * 32 + lane;
-    const int qi = qb * AB + r;                  // query position in the sequence
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const float scale2 = LOG2E * 0.125f;         // log2(e) / sqrt(64)
-    float o[32];                                 // O columns half*32 .. half*32+31
-#pragma unroll
-    for (int c = 0; c < 32; ++c) o[c] = 0.0f;
-    float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
+    const uint32_t tSw = tbase + F_S + 128 * w + lane_off;
+    const uint32_t tPw = tbase + F_P + 64 * w + lane_off;
+    const uint32_t tOw = tbase + F_O + 64 * w + lane_off;
+    const float scale2 = LOG2E * 0.125f;      // log2(e) / sqrt(64)
     bool ok = true;
-    // Every thread passes the same named barriers, also after a failed wait,
-    // so that a timeout never leaves the other warps blocked at a barrier.
-    for (int j = 0; j < nkb; ++j) {
-      ok = ok && mbar_wait(s_full, j & 1);
-      const bool diag = (j == qb);
-      uint32_t sr[2][32];
-      float mx = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32_async(tS + lane_off + half * 64, sr[0]);
-        tmem_ld32_async(tS + lane_off + half * 64 + 32, sr[1]);
-        tmem_wait();
-        tc_fence_before();
-        mbar_arrive(s_free);                       // S is in registers: the next QK^T may start
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if (half * 64 + c * 32 + t <= r) mx = fmaxf(mx, __uint_as_float(sr[c][t]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(sr[c][t]));
+    int c = 0;
+    FwdUnit U;
+    for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
+      const int nw = w ? U.n1 : U.n0;
+      if (nw == 0) continue;
+      const int qb = 2 * U.p + w;
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nw; ++j, ++c) {
+        if (!mbar_wait(&s_full[w], c & 1)) {
+          ok = false;
+          break;
         }
-      }
-      float* rm = red_max + (j & 1) * 2 * AB;
-      rm[half * AB + r] = mx;
-      named_sync(1, NSWT);
-      if (!ok) continue;
-      mx = fmaxf(rm[r], rm[AB + r]);
-      const float m_new = fmaxf(m, mx * scale2);
-      const float alpha = exp2f(m - m_new);
-      if (j > 0) {   // fold in O_{j-1}; its MMA has also finished reading P
-        ok = mbar_wait(&o_full[(j - 1) & 1], ((j - 1) >> 1) & 1);
-        if (!ok) continue;
         tc_fence_after();
-        float v[32];
-        tmem_ld32(tO0 + ((j - 1) & 1) * 64 + half * 32 + lane_off, v);
+        const bool diag = (j == qb);
+        uint32_t buf[2][32];
+        // pass 1: the row maximum (four 32-column chunks, next load in flight)
+        float pm[8];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = o[t] * alpha_prev + v[t];
-        tc_fence_before();
-        mbar_arrive(&o_free[(j - 1) & 1]);
-      }
-      float lsum = 0.0f;
+        for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
+        tmem_ld32_async(tSw, buf[0]);
+        tmem_wait_regs(buf[0]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t(&cur)[32] = buf[ch & 1];
+          if (ch < 3) tmem_ld32_async(tSw + 32 * (ch + 1), buf[(ch + 1) & 1]);
+          if (diag) mask_diag(cur, ch * 32, r);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          float e = exp2f(__uint_as_float(sr[c][t]) * scale2 - m_new);
-          if (diag && half * 64 + c * 32 + t > r) e = 0.0f;
-          sr[c][t] = __float_as_uint(e);
-          lsum += e;
+          for (int e = 0; e < 32; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(cur[e]));
+          if (ch < 3) tmem_wait_regs(buf[(ch + 1) & 1]);
         }
-        store_row_chunk_bits(sP, r, (half * 2 + c) * 4, sr[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale2;
+        const bool need = mx > m + RESCALE_T;
+        const float m_new = need ? mx : m;
+        const float alpha = need ? exp2f(m - m_new) : 1.0f;
+        // P_w and O_w are free once the previous P V product is done
+        if (c > 0 && !mbar_wait(&o_done[w], (c - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // pass 2: P = 2^(s scale2 - m_new) as bf16 pairs into TMEM; row sum
+        const float2 sc2 = make_float2(scale2, scale2), nm2 = make_float2(-m_new, -m_new);
+        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+        tmem_ld32_async(tSw, buf[0]);
+        tmem_wait_regs(buf[0]);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t(&cur)[32] = buf[ch & 1];
+          if (ch < 3) tmem_ld32_async(tSw + 32 * (ch + 1), buf[(ch + 1) & 1]);
+          if (diag) mask_diag(cur, ch * 32, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 y = __ffma2_rn(u2f2(cur[e], cur[e + 1]), sc2, nm2);
+            const float2 pe = make_float2(ex2(y.x), ex2(y.y));
+            ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], pe);
+            __nv_bfloat162 hv = __floats2bfloat162_rn(pe.x, pe.y);
+            pk[e >> 1] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          tmem_st16(tPw + 16 * ch, pk);
+          if (ch < 3) tmem_wait_regs(buf[(ch + 1) & 1]);
+        }
+        const float2 lsp = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+        // O = O * alpha for the rows whose reference maximum moved
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t ov[32];
+            tmem_ld32_async(tOw + 32 * hh, ov);
+            tmem_wait_regs(ov);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 sc = __fmul2_rn(u2f2(ov[e], ov[e + 1]), a2);
+              ov[e] = __float_as_uint(sc.x);
+              ov[e + 1] = __float_as_uint(sc.y);
+            }
+            tmem_st16(tOw + 32 * hh, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+            tmem_st16(tOw + 32 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[w]);
+        l = l * alpha + (lsp.x + lsp.y);
+        m = m_new;
       }
-      fence_proxy_async();
-      mbar_arrive(p_full);
-      l = l * alpha + lsum;
-      m = m_new;
-      alpha_prev = alpha;
-    }
-    ok = ok && mbar_wait(&o_full[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1);
-    if (ok) {
+      if (!ok) break;
+      // unit end: O_w / l -> bf16 output; LSE
+      if (!mbar_wait(&o_done[w], (c - 1) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      float v[32];
-      tmem_ld32(tO0 + ((nkb - 1) & 1) * 64 + half * 32 + lane_off, v);
+      const int qi = qb * AB + r;
+      const int row0 = U.b * A.S;
+      bf16* out = A.o + (size_t)(row0 + qi) * d + U.h * AD;
+      const float inv = 1.0f / l;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) o[t] = o[t] * alpha_prev + v[t];
+      for (int hh = 0; hh < 2; ++hh) {
+        float ov[32];
+        tmem_ld32(tOw + 32 * hh, ov);
+        store8_bf16_row(out + 32 * hh, ov, inv);
+      }
+      A.lse[((size_t)U.b * A.H + U.h) * A.S + qi] = (m + log2f(l)) / LOG2E;
+      tc_fence_before();
+      mbar_arrive(&o_free[w]);
     }
-    red_l[half * AB + r] = l;
-    named_sync(1, NSWT);
-    if (ok) {
-      const float lt = red_l[r] + red_l[AB + r];
-      const float inv = 1.0f / lt;
-      store8_bf16_row(A.o + (size_t)(row0 + qi) * d + h * AD + half * 32, o, inv);
-      if (half == 0) A.lse[((size_t)b * A.H + h) * A.S + qi] = (m + log2f(lt)) / LOG2E;
-    } else {
-      fail_wait(A.err, abort_flag);
-    }
+    if (!ok) fail_wait(A.err, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(*tmem_slot, 256);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -452,27 +567,40 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const bool diag = (t == 0);                // query block jb holds the diagonal
       const float* L = sL + bf * AB;
       const float* Dv = sD + bf * AB;
+      const float2 sc2 = make_float2(scale2, scale2), nlog2 = make_float2(-LOG2E, -LOG2E);
 #pragma unroll 1
       for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
-        float s[32], dp[32];
-        tmem_ld32(tSt + lane_off + c4 * 32, s);
-        tmem_ld32(tdPt + lane_off + c4 * 32, dp);
+        uint32_t s[32], dp[32];
+        tmem_ld32_async(tSt + lane_off + c4 * 32, s);
+        tmem_ld32_async(tdPt + lane_off + c4 * 32, dp);
+        tmem_wait();
+        if (diag) {   // queries before the key get -inf, so their 2^x is 0
+          const int lim = r - c4 * 32;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < lim) s[e] = 0xff800000u;
+        }
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 l4 = reinterpret_cast<const float4*>(L + c4 * 32)[e4];
           const float4 d4 = reinterpret_cast<const float4*>(Dv + c4 * 32)[e4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 4; u += 2) {
             const int e = e4 * 4 + u;
-            float p = exp2f(s[e] * scale2 - lv[u] * LOG2E);
-            if (diag && c4 * 32 + e < r) p = 0.0f;     // query < key
-            s[e] = p;
-            dp[e] = p * (dp[e] - dv[u]);
+            const float2 l2 = u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+            const float2 d2 = u ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            // p = 2^(s * log2(e) / 8 - LSE * log2(e)), dS = p (dP - D)
+            const float2 y = __ffma2_rn(u2f2(s[e], s[e + 1]), sc2, __fmul2_rn(l2, nlog2));
+            const float2 pp = make_float2(ex2(y.x), ex2(y.y));
+            const float2 ds = __fmul2_rn(pp, __fadd2_rn(u2f2(dp[e], dp[e + 1]), d2));
+            s[e] = __float_as_uint(pp.x);
+            s[e + 1] = __float_as_uint(pp.y);
+            dp[e] = __float_as_uint(ds.x);
+            dp[e + 1] = __float_as_uint(ds.y);
           }
         }
-        store_row_chunk(sPt, r, c4 * 4, s);
-        store_row_chunk(sdSt, r, c4 * 4, dp);
+        store_row_chunk_bits(sPt, r, c4 * 4, s);
+        store_row_chunk_bits(sdSt, r, c4 * 4, dp);
       }
       tc_fence_before();
       mbar_arrive(st_free);
@@ -622,17 +750,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         ok = false;
         break;
       }
-      const bool diag = (t == ib);
+      if (t == ib) {   // keys after the query get -inf, so their 2^x is 0
+        const int lim = r - half * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e > lim) sr[c][e] = 0xff800000u;
+      }
+      // p = 2^(s * log2(e) / 8 - LSE * log2(e)), dS = p (dP - D), two lanes at a time
+      const float2 sc2 = make_float2(scale2, scale2), nl2 = make_float2(-L2, -L2),
+                   nd2 = make_float2(-Di, -Di);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int c4 = half * 2 + c;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float p = exp2f(__uint_as_float(sr[c][e]) * scale2 - L2);
-          if (diag && c4 * 32 + e > r) p = 0.0f;      // key > query
-          dr[c][e] = __float_as_uint(p * (__uint_as_float(dr[c][e]) - Di));
+        for (int e = 0; e < 32; e += 2) {
+          const float2 y = __ffma2_rn(u2f2(sr[c][e], sr[c][e + 1]), sc2, nl2);
+          const float2 pp = make_float2(ex2(y.x), ex2(y.y));
+          const float2 ds = __fmul2_rn(pp, __fadd2_rn(u2f2(dr[c][e], dr[c][e + 1]), nd2));
+          dr[c][e] = __float_as_uint(ds.x);
+          dr[c][e + 1] = __float_as_uint(ds.y);
         }
-        store_row_chunk_bits(sdS, r, c4 * 4, dr[c]);
+        store_row_chunk_bits(sdS, r, (half * 2 + c) * 4, dr[c]);
       }
       fence_proxy_async();
       mbar_arrive(ds_full);
@@ -687,7 +826,7 @@ bool map_128x64(CUtensorMap* m, const void* base, long long rows, long long cols
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t SMEM_FWD = 1024 + TILE * 5 + PTILE + 128 + 6 * AB * 4;
+constexpr size_t SMEM_FWD = 1024 + TILE * (4 + 2 * FWD_NST) + 256;
 constexpr size_t SMEM_DKDV = 1024 + TILE * 6 + 2 * PTILE + 4 * AB * 4 + 128;
 constexpr size_t SMEM_DQ = 1024 + TILE * 6 + PTILE + 128;
 
@@ -714,7 +853,11 @@ cudaError_t attn_fwd_tc_launch(const void* qkv, void* o, float* lse, int nb, int
   CUtensorMap m;
   if (!map_128x64(&m, qkv, (long long)nb * S, 3LL * H * AD, 3LL * H * AD)) return cudaErrorInvalidValue;
   AttnArgs a{S, H, (bf16*)o, lse, nullptr, nullptr, err};
-  attn_fwd_tc<<<dim3(S / AB, H, nb), AT_THREADS, SMEM_FWD, s>>>(m, a);
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int units = ((S / AB + 1) / 2) * H * nb;
+  attn_fwd_tc<<<units < sms ? units : sms, FWD_THREADS, SMEM_FWD, s>>>(m, a, nb);
   return cudaGetLastError();
 }
 

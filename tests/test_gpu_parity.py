@@ -30,7 +30,25 @@ def ragged():
                       lr=1e-3, steps=3, init="he_normal", x_dist="normal")
 
 
+def attn(seq: int, heads: int, nseq: int, name: str):
+    """One causal attention layer (head_dim 64) between two projections, MSE,
+    Adam: sequence lengths with an odd number of 128-row blocks, a single
+    block, more (pair, head, sequence) units than SMs, and a length that is
+    not a multiple of 128."""
+    d = heads * 64
+    return W.Workload(name=name, index=11, batch=seq * nseq,
+                      layers=[W.linear(d, 3 * d, False), W.causal_attention(heads, 64, seq),
+                              W.linear(d, d, False)],
+                      loss="mse", precisions=("bf16",), optimizer="adam", lr=1e-3,
+                      steps=2, init="normal002", x_dist="normal")
+
+
 CASES = {
+    "attn_s128_h3_b2": (lambda: attn(128, 3, 2, "attn_s128"), "bf16", 2),
+    "attn_s384_h5_b3": (lambda: attn(384, 5, 3, "attn_s384"), "bf16", 2),
+    "attn_s640_h2_b2": (lambda: attn(640, 2, 2, "attn_s640"), "bf16", 2),
+    "attn_s256_h8_b24": (lambda: attn(256, 8, 24, "attn_s256"), "bf16", 2),
+    "attn_s192_h2_b2": (lambda: attn(192, 2, 2, "attn_s192"), "bf16", 2),
     "c1": (lambda: W.workload("c1"), "strict", 1),
     "c2_strict": (lambda: W.workload("c2"), "strict", 10),
     "c2_bf16": (lambda: W.workload("c2"), "bf16", 10),
