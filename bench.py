@@ -26,9 +26,14 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-# DRAM bytes per launch of the dominant kernel from one ncu capture of the
-# current code (profiles/), keyed by kernel family; None when not captured.
-TRAFFIC = {}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
+# kernel family, averaged over the launches of one training step, from one ncu
+# capture of the current code (summary and command under profiles/); keyed by
+# (workload, family); None when not captured for that pair.
+TRAFFIC = {
+    # C3: the ten SM-pair GEMM launches of one step (fwd, dX, dW shapes)
+    ("c3_mlp4096_gelu", "gemm_pair_kernel (tcgen05 cta_group::2)"): 249.55e6,
+}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (maximum SM clock)
@@ -434,7 +439,7 @@ def main():
         "roofline": {"kernel": top["name"], "launches_timed": top["launches"],
                      "share": top["total_ms"] / total_prof if total_prof else None,
                      "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": TRAFFIC.get(top["name"]),
+                     "unit": unit, "frac": achieved / peak, "traffic": TRAFFIC.get((w.name, top["name"])),
                      "peak_note": f"{'sustained bf16' if bound == 'tensor' else bound} peak, {peak_src}"},
         "kernels": kernels,
         "kernel_families": [{"kernel": f["name"], "launches": f["launches"],
