@@ -8,15 +8,16 @@
 // D_i = sum_c dO_ic O_ic:  P = exp(S - LSE), dP = dO V^T, dS = P (dP - D),
 // dV = P^T dO, dK = dS^T Q / 8, dQ = dS K / 8.
 //
-// Every kernel: one CTA per (128-row block, head, sequence), 288 threads.
-// Warp 0 lane 0 issues TMA loads and tcgen05.mma; warps 1-8 each own one TMEM
-// lane quarter (32 rows of the 128-row block) and one half of the 128 columns,
-// read S / dP with tcgen05.ld, do the softmax arithmetic in fp32 and write bf16
-// P / dS tiles into shared memory in the 128-byte-swizzled K-major layout the
-// next MMA reads.  The two warps that share a row exchange its maximum through
-// shared memory (forward only).
-//   forward: S = Q K_j^T (TMEM) -> P (smem) -> O_j = P V_j (TMEM, two slots);
-//            O, the running max and sum stay in registers (online softmax).
+// Forward: persistent, one CTA per SM over (query block, head, sequence)
+// units; S, P and O live in tensor memory (P is the A operand of P V, read from
+// TMEM) and two softmax groups take alternate key blocks with their own
+// running maximum and sum, merged at the end of the unit (see below).
+// Backward: one CTA per (128-row block, head, sequence), 288 threads.  Warp 0
+// lane 0 issues TMA loads and tcgen05.mma; warps 1-8 each own one TMEM lane
+// quarter (32 rows of the 128-row block) and one half of the 128 columns, read
+// S / dP with tcgen05.ld, do the arithmetic in fp32 and write bf16 P / dS
+// tiles into shared memory in the 128-byte-swizzled K-major layout the next
+// MMA reads.
 //   dK/dV:   per key block, over the query blocks that see it:
 //            S^T = K Q_i^T and dP^T = V dO_i^T (keys are the M dimension), so
 //            P^T and dS^T are written row by row and feed dV += P^T dO_i and
@@ -111,6 +112,29 @@ __device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) {
   return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
+// 2^x for two lanes on the FMA and integer pipes, which the special-function
+// unit's ex2 leaves idle: 2^x = 2^j 2^f with j = round(x) (adding 1.5 * 2^23
+// rounds to an integer and leaves j in the low mantissa bits), f = x - j in
+// [-1/2, 1/2], 2^f from a cubic fitted for least maximum relative error by
+// Lawson's iteratively reweighted least squares (8.4e-5, below bf16 rounding),
+// and j added into the exponent field.  x is clamped below at -125, so keys
+// masked with -inf give ~2^-125 instead of 0: nothing at bf16 resolution.
+__device__ __forceinline__ float2 ex2_poly2(float2 x) {
+  constexpr float RND = 12582912.0f;
+  constexpr float C0 = 0.999919593334198f, C1 = 0.6932621598243713f,
+                  C2 = 0.24271413683891296f, C3 = 0.055212993174791336f;
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 t = __fadd2_rn(x, make_float2(RND, RND));
+  const float2 j = __fadd2_rn(t, make_float2(-RND, -RND));
+  const float2 f = __ffma2_rn(j, make_float2(-1.0f, -1.0f), x);
+  float2 p = __ffma2_rn(make_float2(C3, C3), f, make_float2(C2, C2));
+  p = __ffma2_rn(p, f, make_float2(C1, C1));
+  p = __ffma2_rn(p, f, make_float2(C0, C0));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
 constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
 constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
 
@@ -134,37 +158,38 @@ __device__ __forceinline__ void store_row_chunk_bits(uint8_t* ptile, int r, int 
 }
 
 // ============================================================ forward
-// Persistent, one CTA per SM.  A work unit is a pair of consecutive query
-// blocks (2p, 2p+1) of one (head, sequence).  Warps 0-3 own query block 2p
-// (tile 0) and warps 4-7 block 2p+1 (tile 1), one query row per thread; warp 8
-// is the TMA producer, warp 9 issues the MMAs.  Per key block j and tile w:
-//   S_w = Q_w K_j^T          TMEM, fp32, 128 columns
-//   P_w = 2^(S_w/8 log2e - m) TMEM, bf16 pairs, 64 columns
-//   O_w += P_w V_j           TMEM, fp32, 64 columns (A operand read from TMEM)
-// While one tile's softmax runs, the tensor core works on the other tile.
-// m is the row's reference maximum (log2 units); it is raised, and O and l
-// rescaled, only when a block's maximum exceeds it by more than 8, so that
-// P <= 2^8.  Tile 0 skips key block 2p+1, which lies after all its queries.
-// Units are dealt to the CTAs heaviest first in snake order.
+// Persistent, one CTA per SM; a work unit is one 128-row query block of one
+// (head, sequence), dealt to the CTAs heaviest first in snake order.  Warp 8
+// is the TMA producer, warp 9 issues the MMAs, warps 0-7 do the softmax in
+// two groups: group p (warps 4p .. 4p+3, one query row per thread) takes the
+// key blocks whose running index g has parity p, with its own buffers
+//   S[p] = Q K_g^T            TMEM, fp32, 128 columns
+//   P[p] = 2^(S/8 log2e - m)  TMEM, bf16 pairs, 64 columns
+//   O[p] += P[p] V_g          TMEM, fp32, 64 columns (A operand read from TMEM)
+// and its own running maximum m and sum l, so the two groups never wait for
+// each other inside a unit (their warps share the SM sub-partitions and fill
+// each other's latencies).  At the end of a unit the two partial results are
+// merged: M = max(m0, m1), O = (O0 2^(m0-M) + O1 2^(m1-M)) / (l0 2^(m0-M) +
+// l1 2^(m1-M)).  m is a reference maximum in log2 units; it is raised, and
+// O[p] and l rescaled, only when a block's maximum exceeds it by more than 8,
+// so that P <= 2^8.
 constexpr int FWD_THREADS = 320;
-constexpr int FWD_NST = 3;                            // K/V ring stages
-constexpr uint32_t F_S = 0, F_P = 256, F_O = 384;     // TMEM columns of S, P, O (tile 0)
+constexpr int FWD_NST = 3;                                  // K/V ring stages
+constexpr uint32_t F_S = 0, F_P = 256, F_O = 384;           // TMEM columns of S[0], P[0], O[0]
 constexpr float RESCALE_T = 8.0f;
 
 struct FwdUnit {
-  int p, h, b, n0, n1;   // pair, head, sequence; key blocks of tile 0 / tile 1 (0: no tile 1)
+  int qb, h, b;   // query block, head, sequence; key blocks 0 .. qb
 };
 
-__device__ __forceinline__ bool fwd_unit(int k, int n_units, int npair, int nqb, int H, FwdUnit& U) {
+__device__ __forceinline__ bool fwd_unit(int k, int n_units, int nqb, int H, FwdUnit& U) {
   const int G = gridDim.x;
   const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
   if (u >= n_units) return false;
-  const int hb = n_units / npair;
-  U.p = npair - 1 - u / hb;
+  const int hb = n_units / nqb;
+  U.qb = nqb - 1 - u / hb;
   U.h = (u % hb) % H;
   U.b = (u % hb) / H;
-  U.n0 = 2 * U.p + 1;
-  U.n1 = (2 * U.p + 1 < nqb) ? 2 * U.p + 2 : 0;
   return true;
 }
 
@@ -176,23 +201,27 @@ __device__ __forceinline__ void mask_diag(uint32_t (&v)[32], int col0, int r) {
     if (col0 + e > r) v[e] = 0xff800000u;
 }
 
+// Barrier between the two warps that share a TMEM lane quarter (ids 1-4).
+__device__ __forceinline__ void pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sQ = sm;                          // [2 slots][2 tiles]
-  uint8_t* sK = sQ + 4 * TILE;               // [FWD_NST]
+  uint8_t* sQ = sm;                          // [2 slots]
+  uint8_t* sK = sQ + 2 * TILE;               // [FWD_NST]
   uint8_t* sV = sK + FWD_NST * TILE;         // [FWD_NST]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sV + FWD_NST * TILE);
   uint64_t *q_full = bar, *q_empty = bar + 2, *kv_full = bar + 4, *kv_empty = kv_full + FWD_NST;
-  uint64_t *s_full = kv_empty + FWD_NST, *p_full = s_full + 2, *o_done = s_full + 4,
-           *o_free = s_full + 6;
+  uint64_t *s_full = kv_empty + FWD_NST, *s_free = s_full + 2, *p_full = s_full + 4,
+           *o_done = s_full + 6, *o_free = s_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
+  float* xch = reinterpret_cast<float*>(bar + 32);    // [m, l][2 groups][128]: unit-end merge
   const int nqb = A.S / AB;
-  const int npair = (nqb + 1) / 2;
-  const int n_units = npair * A.H * nb;
+  const int n_units = nqb * A.H * nb;
   const int d = A.H * AD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -201,10 +230,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], NSWT / 2);     // one softmax group
+      mbar_init(&p_full[i], NSWT / 2);
       mbar_init(&o_done[i], 1);
-      mbar_init(&o_free[i], 128);
     }
+    mbar_init(o_free, NSWT);                // both groups
     for (int i = 0; i < FWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
@@ -224,17 +254,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       bool ok = true;
       int g = 0;
       FwdUnit U;
-      for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
+      for (int k = 0; ok && fwd_unit(k, n_units, nqb, A.H, U); ++k) {
         const int row0 = U.b * A.S, slot = k & 1;
-        const int nmax = U.n1 ? U.n1 : U.n0;
         ok = mbar_wait(&q_empty[slot], ((k >> 1) & 1) ^ 1);
         if (!ok) break;
-        mbar_expect_tx(&q_full[slot], (U.n1 ? 2 : 1) * TILE);
-        tma_load_2d(sQ + (2 * slot) * TILE, &tm_qkv, &q_full[slot], U.h * AD, row0 + 2 * U.p * AB);
-        if (U.n1)
-          tma_load_2d(sQ + (2 * slot + 1) * TILE, &tm_qkv, &q_full[slot], U.h * AD,
-                      row0 + (2 * U.p + 1) * AB);
-        for (int j = 0; j < nmax; ++j, ++g) {
+        mbar_expect_tx(&q_full[slot], TILE);
+        tma_load_2d(sQ + slot * TILE, &tm_qkv, &q_full[slot], U.h * AD, row0 + U.qb * AB);
+        for (int j = 0; j <= U.qb; ++j, ++g) {
           const int st = g % FWD_NST;
           ok = mbar_wait(&kv_empty[st], ((g / FWD_NST) & 1) ^ 1);
           if (!ok) break;
@@ -248,156 +274,159 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      bool ok = true;
-      int g = 0;
-      int c[2] = {0, 0};     // S/P iterations issued per tile
-      int uo[2] = {0, 0};    // units started per tile
-      // the previous step, whose P V products are still to be issued
-      int pv_st = -1, pv_act = 0, pv_first = 0;
-      auto issue_pv = [&](int w) -> bool {
-        // P_w of tile-iteration c[w]-1 is complete (this also frees S_w)
-        if (!mbar_wait(&p_full[w], (c[w] - 1) & 1)) return false;
-        if ((pv_first >> w) & 1) {
-          if (uo[w] > 1 && !mbar_wait(&o_free[w], (uo[w] - 2) & 1)) return false;
-        }
-        tc_fence_after();
-        const uint8_t* v = sV + pv_st * TILE;
-#pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16_ts(tbase + F_O + 64 * w, tbase + F_P + 64 * w + kk * 8, mndesc(v, kk),
-                      IDESC_128x64_KMN, !(((pv_first >> w) & 1) && kk == 0));
-        mma_commit(&o_done[w]);
-        return true;
+      // descriptors of the first tile of each buffer; a tile further is
+      // TILE >> 4 further, a K step 32 bytes (K-major) or 16 rows (V, MN-major)
+      constexpr uint64_t TSTEP = TILE >> 4;
+      const uint64_t dq0 = kdesc(sQ, 0), dk0 = kdesc(sK, 0), dv0 = mndesc(sV, 0);
+      // Two cursors walk the same sequence of (unit, key block): one issues
+      // S = Q K^T as soon as the block's K/V and S buffer are ready, the
+      // other P V as soon as the block's P is; neither waits on the other's
+      // barriers, so the tensor core gets whichever product is ready first.
+      struct Cursor {
+        int k, j, g;
+        FwdUnit U;
+        bool valid;
       };
-      FwdUnit U;
-      for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
-        const int slot = k & 1;
-        const int nmax = U.n1 ? U.n1 : U.n0;
-        ok = mbar_wait(&q_full[slot], (k >> 1) & 1);
-        for (int j = 0; ok && j < nmax; ++j, ++g) {
-          const int st = g % FWD_NST;
-          const int act = (j < U.n0 ? 1 : 0) | (j < U.n1 ? 2 : 0);
-          ok = mbar_wait(&kv_full[st], (g / FWD_NST) & 1);
-          if (!ok) break;
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            if ((pv_act >> w) & 1) {
-              ok = issue_pv(w);
-              if (!ok) break;
-            }
-            if ((act >> w) & 1) {
-              tc_fence_after();
-              const uint8_t* q = sQ + (2 * slot + w) * TILE;
-              const uint8_t* kt = sK + st * TILE;
-#pragma unroll
-              for (int kk = 0; kk < AD / 16; ++kk)
-                mma_bf16(tbase + F_S + 128 * w, kdesc(q, kk), kdesc(kt, kk), IDESC_128x128_KK, kk > 0);
-              mma_commit(&s_full[w]);
-              ++c[w];
-            }
-          }
-          if (!ok) break;
-          if (pv_act) mma_commit(&kv_empty[pv_st]);
-          if (j == nmax - 1) mma_commit(&q_empty[slot]);
-          if (j == 0) {   // counted after the previous unit's last P V products
-            if (U.n0) ++uo[0];
-            if (U.n1) ++uo[1];
-          }
-          pv_st = st;
-          pv_act = act;
-          pv_first = (j == 0) ? act : 0;
+      auto advance = [&](Cursor& c) {
+        ++c.g;
+        if (++c.j > c.U.qb) {
+          c.j = 0;
+          ++c.k;
+          c.valid = fwd_unit(c.k, n_units, nqb, A.H, c.U);
         }
-      }
-      if (ok && pv_act) {
-        for (int w = 0; w < 2 && ok; ++w)
-          if ((pv_act >> w) & 1) ok = issue_pv(w);
-        if (ok) mma_commit(&kv_empty[pv_st]);
+      };
+      Cursor cq, cp;
+      cq.k = cq.j = cq.g = 0;
+      cq.valid = fwd_unit(0, n_units, nqb, A.H, cq.U);
+      cp = cq;
+      bool ok = true;
+      uint32_t idle = 0;
+      while (cp.valid) {
+        bool did = false;
+        if (cq.valid) {
+          const int st = cq.g % FWD_NST, sb = cq.g & 1, slot = cq.k & 1;
+          // S[sb] was last read by its group two blocks ago
+          if ((cq.j > 0 || mbar_test(&q_full[slot], (cq.k >> 1) & 1)) &&
+              mbar_test(&kv_full[st], (cq.g / FWD_NST) & 1) &&
+              (cq.g < 2 || mbar_test(&s_free[sb], ((cq.g - 2) >> 1) & 1))) {
+            tc_fence_after();
+            const uint64_t aq = dq0 + (uint64_t)slot * TSTEP;
+            const uint64_t bk = dk0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AD / 16; ++kk)
+              mma_bf16(tbase + F_S + 128 * sb, aq + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
+            mma_commit(&s_full[sb]);
+            if (cq.j == cq.U.qb) mma_commit(&q_empty[slot]);
+            advance(cq);
+            did = true;
+          }
+        }
+        if (cp.g < cq.g) {
+          const int pb = cp.g & 1;
+          // a unit's first product overwrites O: the previous unit's O is read out
+          if (mbar_test(&p_full[pb], (cp.g >> 1) & 1) &&
+              (cp.j != 0 || cp.k == 0 || mbar_test(o_free, (cp.k - 1) & 1))) {
+            tc_fence_after();
+            const int st = cp.g % FWD_NST;
+            const uint64_t bv = dv0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AB / 16; ++kk)
+              mma_bf16_ts(tbase + F_O + 64 * pb, tbase + F_P + 64 * pb + kk * 8, bv + kk * 128,
+                          IDESC_128x64_KMN, kk > 0 || cp.j >= 2);
+            mma_commit(&o_done[pb]);
+            mma_commit(&kv_empty[st]);
+            advance(cp);
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
   } else {
-    // ---------------- softmax: warps 0-3 tile 0, warps 4-7 tile 1 ----------------
-    const int w = warp >> 2;
+    // ---------------- softmax: two groups of four warps ----------------
     const int quarter = warp & 3;
+    const int grp = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tSw = tbase + F_S + 128 * w + lane_off;
-    const uint32_t tPw = tbase + F_P + 64 * w + lane_off;
-    const uint32_t tOw = tbase + F_O + 64 * w + lane_off;
+    const uint32_t tS = tbase + F_S + 128 * grp + lane_off;
+    const uint32_t tP = tbase + F_P + 64 * grp + lane_off;
+    const uint32_t tO = tbase + F_O + 64 * grp + lane_off;
     const float scale2 = LOG2E * 0.125f;      // log2(e) / sqrt(64)
     bool ok = true;
-    int c = 0;
+    int g0 = 0;                               // running index of the unit's first block
     FwdUnit U;
-    for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
-      const int nw = w ? U.n1 : U.n0;
-      if (nw == 0) continue;
-      const int qb = 2 * U.p + w;
+    // Both groups pass the unit-end barrier, also after a failed wait, so
+    // that a timeout never leaves the partner warp blocked there.
+    for (int k = 0; fwd_unit(k, n_units, nqb, A.H, U); ++k) {
+      const int n = U.qb + 1;
       float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nw; ++j, ++c) {
-        if (!mbar_wait(&s_full[w], c & 1)) {
+      int last = -1;                          // running index of this group's last block
+      for (int j = (grp - g0) & 1; ok && j < n; j += 2) {
+        const int gi = g0 + j;
+        if (!mbar_wait(&s_full[grp], (gi >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool diag = (j == qb);
-        uint32_t buf[2][32];
-        // pass 1: the row maximum (four 32-column chunks, next load in flight)
+        // the whole 128-column row of S in registers, then S[grp] is released
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32_async(tS + 32 * ch, sv[ch]);
+        tmem_wait_regs(sv[0]);
+        reg_fence(sv[1]);
+        reg_fence(sv[2]);
+        reg_fence(sv[3]);
+        tc_fence_before();
+        mbar_arrive(&s_free[grp]);
+        if (j == U.qb) {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) mask_diag(sv[ch], 32 * ch, r);
+        }
         float pm[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
-        tmem_ld32_async(tSw, buf[0]);
-        tmem_wait_regs(buf[0]);
+        for (int e = 0; e < 8; ++e) pm[e] = __uint_as_float(sv[0][e]);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t(&cur)[32] = buf[ch & 1];
-          if (ch < 3) tmem_ld32_async(tSw + 32 * (ch + 1), buf[(ch + 1) & 1]);
-          if (diag) mask_diag(cur, ch * 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(cur[e]));
-          if (ch < 3) tmem_wait_regs(buf[(ch + 1) & 1]);
-        }
+        for (int e = 8; e < 128; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
         const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale2;
         const bool need = mx > m + RESCALE_T;
         const float m_new = need ? mx : m;
         const float alpha = need ? exp2f(m - m_new) : 1.0f;
-        // P_w and O_w are free once the previous P V product is done
-        if (c > 0 && !mbar_wait(&o_done[w], (c - 1) & 1)) {
+        // P[grp] and O[grp] are free once this group's previous P V is done
+        if (gi >= 2 && !mbar_wait(&o_done[grp], ((gi - 2) >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // pass 2: P = 2^(s scale2 - m_new) as bf16 pairs into TMEM; row sum
         const float2 sc2 = make_float2(scale2, scale2), nm2 = make_float2(-m_new, -m_new);
-        float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                        make_float2(0.f, 0.f)};
-        tmem_ld32_async(tSw, buf[0]);
-        tmem_wait_regs(buf[0]);
+        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          uint32_t(&cur)[32] = buf[ch & 1];
-          if (ch < 3) tmem_ld32_async(tSw + 32 * (ch + 1), buf[(ch + 1) & 1]);
-          if (diag) mask_diag(cur, ch * 32, r);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 y = __ffma2_rn(u2f2(cur[e], cur[e + 1]), sc2, nm2);
-            const float2 pe = make_float2(ex2(y.x), ex2(y.y));
-            ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], pe);
+            const float2 y = __ffma2_rn(u2f2(sv[ch][e], sv[ch][e + 1]), sc2, nm2);
+            // one pair in four on the FMA pipe, the rest on the SFU
+            const float2 pe = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
+            ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], pe);
             __nv_bfloat162 hv = __floats2bfloat162_rn(pe.x, pe.y);
             pk[e >> 1] = *reinterpret_cast<uint32_t*>(&hv);
           }
-          tmem_st16(tPw + 16 * ch, pk);
-          if (ch < 3) tmem_wait_regs(buf[(ch + 1) & 1]);
+          tmem_st16(tP + 16 * ch, pk);
         }
-        const float2 lsp = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
-        // O = O * alpha for the rows whose reference maximum moved
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O[grp] = O[grp] * alpha for the rows whose reference maximum moved
+        if (last >= 0 && __any_sync(0xffffffffu, need)) {
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t ov[32];
-            tmem_ld32_async(tOw + 32 * hh, ov);
+            tmem_ld32_async(tO + 32 * hh, ov);
             tmem_wait_regs(ov);
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
@@ -405,36 +434,55 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
               ov[e] = __float_as_uint(sc.x);
               ov[e + 1] = __float_as_uint(sc.y);
             }
-            tmem_st16(tOw + 32 * hh, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-            tmem_st16(tOw + 32 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+            tmem_st16(tO + 32 * hh, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+            tmem_st16(tO + 32 * hh + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
           }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[w]);
+        mbar_arrive(&p_full[grp]);
+        const float2 lsp = __fadd2_rn(ls[0], ls[1]);
         l = l * alpha + (lsp.x + lsp.y);
         m = m_new;
+        last = gi;
       }
-      if (!ok) break;
-      // unit end: O_w / l -> bf16 output; LSE
-      if (!mbar_wait(&o_done[w], (c - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int qi = qb * AB + r;
-      const int row0 = U.b * A.S;
-      bf16* out = A.o + (size_t)(row0 + qi) * d + U.h * AD;
-      const float inv = 1.0f / l;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float ov[32];
-        tmem_ld32(tOw + 32 * hh, ov);
-        store8_bf16_row(out + 32 * hh, ov, inv);
-      }
-      A.lse[((size_t)U.b * A.H + U.h) * A.S + qi] = (m + log2f(l)) / LOG2E;
+      // unit end: this group's O is complete once its last P V is done
+      if (ok && last >= 0) ok = mbar_wait(&o_done[grp], (last >> 1) & 1);
+      xch[grp * AB + r] = m;
+      xch[(2 + grp) * AB + r] = l;
       tc_fence_before();
-      mbar_arrive(&o_free[w]);
+      pair_sync(quarter);
+      if (ok) {
+        tc_fence_after();
+        // group p had blocks in this unit unless the unit's only block went to the other
+        const bool has0 = n >= 2 || (g0 & 1) == 0, has1 = n >= 2 || (g0 & 1) == 1;
+        const float m0 = xch[r], m1 = xch[AB + r];
+        const float M = fmaxf(has0 ? m0 : -INFINITY, has1 ? m1 : -INFINITY);
+        const float w0 = has0 ? exp2f(m0 - M) : 0.0f, w1 = has1 ? exp2f(m1 - M) : 0.0f;
+        const float L = (has0 ? xch[2 * AB + r] * w0 : 0.0f) + (has1 ? xch[3 * AB + r] * w1 : 0.0f);
+        // this thread writes head dimensions 32 grp .. +31 of its row
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.0f;
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          if (!(p2 ? has1 : has0)) continue;
+          float ov[32];
+          tmem_ld32(tbase + F_O + 64 * p2 + 32 * grp + lane_off, ov);
+          const float wp = p2 ? w1 : w0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = fmaf(ov[e], wp, o[e]);
+        }
+        const int qi = U.qb * AB + r;
+        store8_bf16_row(A.o + (size_t)(U.b * A.S + qi) * d + U.h * AD + 32 * grp, o, 1.0f / L);
+        if (grp == 0) A.lse[((size_t)U.b * A.H + U.h) * A.S + qi] = (M + log2f(L)) / LOG2E;
+        tc_fence_before();
+      }
+      // xch is rewritten at the next unit's end only after both warps passed
+      // this point (the next pair_sync orders it)
+      pair_sync(quarter);
+      mbar_arrive(o_free);
+      g0 += n;
     }
     if (!ok) fail_wait(A.err, abort_flag);
   }
@@ -826,7 +874,7 @@ bool map_128x64(CUtensorMap* m, const void* base, long long rows, long long cols
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t SMEM_FWD = 1024 + TILE * (4 + 2 * FWD_NST) + 256;
+constexpr size_t SMEM_FWD = 1024 + TILE * (2 + 2 * FWD_NST) + 256 + 4 * AB * 4;
 constexpr size_t SMEM_DKDV = 1024 + TILE * 6 + 2 * PTILE + 4 * AB * 4 + 128;
 constexpr size_t SMEM_DQ = 1024 + TILE * 6 + PTILE + 128;
 
@@ -856,7 +904,7 @@ cudaError_t attn_fwd_tc_launch(const void* qkv, void* o, float* lse, int nb, int
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int units = ((S / AB + 1) / 2) * H * nb;
+  const int units = (S / AB) * H * nb;
   attn_fwd_tc<<<units < sms ? units : sms, FWD_THREADS, SMEM_FWD, s>>>(m, a, nb);
   return cudaGetLastError();
 }

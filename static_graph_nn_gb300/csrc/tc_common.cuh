@@ -45,6 +45,19 @@ static __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
   return false;
 }
 
+// Non-blocking test: has the phase with this parity completed?
+static __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Polling wait with cluster-scope acquire, for barriers that receive arrivals
 // from the other CTA of a pair (remote arrives, multicast commits); bounded,
 // false on timeout.
@@ -155,6 +168,20 @@ static __device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
         "+r"(r[31])
       :
       : "memory");
+}
+
+// Orders every later use of these registers after the preceding statement
+// (an empty statement that the compiler must treat as redefining them).
+static __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane from registers
