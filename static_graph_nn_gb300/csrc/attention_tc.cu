@@ -12,18 +12,11 @@
 // units; S, P and O live in tensor memory (P is the A operand of P V, read from
 // TMEM) and two softmax groups take alternate key blocks with their own
 // running maximum and sum, merged at the end of the unit (see below).
-// Backward: one CTA per (128-row block, head, sequence), 288 threads.  Warp 0
-// lane 0 issues TMA loads and tcgen05.mma; warps 1-8 each own one TMEM lane
-// quarter (32 rows of the 128-row block) and one half of the 128 columns, read
-// S / dP with tcgen05.ld, do the arithmetic in fp32 and write bf16 P / dS
-// tiles into shared memory in the 128-byte-swizzled K-major layout the next
-// MMA reads.
-//   dK/dV:   per key block, over the query blocks that see it:
-//            S^T = K Q_i^T and dP^T = V dO_i^T (keys are the M dimension), so
-//            P^T and dS^T are written row by row and feed dV += P^T dO_i and
-//            dK += dS^T Q_i directly; dV, dK accumulate in TMEM.
-//   dQ:      per query block, over the visible key blocks: S, dP, then
-//            dQ += dS K_j accumulated in TMEM.
+// Backward: the same persistent plan for the dK/dV kernel (per key block,
+// over the query blocks that see it: S^T and dP^T with the keys as the M
+// dimension, P^T and dS^T into TMEM, dV += P^T dO_i and dK += dS^T Q_i) and
+// for the dQ kernel (per query block, over the visible key blocks: S, dP,
+// dS into TMEM, dQ += dS K_j).
 // All mbarrier waits are bounded; on expiry the error word is set and the CTA
 // unwinds.
 #include "common.cuh"
@@ -38,9 +31,7 @@ using namespace tc;
 constexpr int AD = 64;                      // head dimension
 constexpr int AB = 128;                     // rows (queries / keys) per block
 constexpr uint32_t TILE = AB * AD * 2;      // one [128][64] bf16 tile: 16 KB
-constexpr uint32_t PTILE = 2 * TILE;        // one [128][128] bf16 tile: 32 KB (two K atoms)
 constexpr int NSW = 8;                      // softmax / elementwise warps (two per TMEM lane quarter)
-constexpr int AT_THREADS = 32 * (1 + NSW);
 constexpr int NSWT = 32 * NSW;              // their thread count
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -73,10 +64,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // K-major descriptors: a [128 rows][64 cols] tile (SBO 1024); k-step of 16 = 32 bytes.
 __device__ __forceinline__ uint64_t kdesc(const uint8_t* tile, int kstep) {
   return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
-}
-// K-major descriptor into a [128 rows][128 cols] tile stored as two 64-col atoms.
-__device__ __forceinline__ uint64_t kdesc_p(const uint8_t* ptile, int kstep) {
-  return smem_desc(smem_u32(ptile) + (kstep >> 2) * TILE + (kstep & 3) * 32, 16, 1024);
 }
 // MN-major descriptor: the same [128 rows = K][64 cols = N] tile read with K
 // along the rows; k-step of 16 rows = 2048 bytes.
@@ -137,25 +124,6 @@ __device__ __forceinline__ float2 ex2_poly2(float2 x) {
 
 constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
 constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
-
-// 32 fp32 values held as raw bits (computed in place in the TMEM load
-// registers) -> bf16, written as four 16-byte chunks of row r (column chunks
-// cc0..cc0+3 of a two-atom [128][128] tile).
-__device__ __forceinline__ void store_row_chunk_bits(uint8_t* ptile, int r, int cc0, const uint32_t* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int cc = cc0 + q;
-    uint4 u;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(v[q * 8 + 2 * i]),
-                                                __uint_as_float(v[q * 8 + 2 * i + 1]));
-      w[i] = *reinterpret_cast<uint32_t*>(&hv);
-    }
-    *reinterpret_cast<uint4*>(ptile + (cc >> 3) * TILE + sw128(r, cc & 7)) = u;
-  }
-}
 
 // ============================================================ forward
 // Persistent, one CTA per SM; a work unit is one 128-row query block of one
@@ -495,38 +463,93 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   }
 }
 
-// ============================================================ backward dK/dV
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// ============================================================ backward
+// Both backward kernels follow the forward's plan: persistent CTAs over
+// (128-row block, head, sequence) units dealt heaviest first in snake order,
+// warp 8 the TMA producer, warp 9 an event-driven MMA issuer, warps 0-7 the
+// elementwise work (warp w: TMEM lane quarter w & 3, columns 64 (w >> 2) ..
+// +63), S and dP read from TMEM once and released, and the bf16 products P /
+// dS written back into TMEM as the A operand of the accumulating MMAs.
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_NST = 3;   // ring stages of the streamed operand pair
+
+__device__ __forceinline__ bool bwd_unit(int k, int n_units, int hb, int H, int& major, int& h,
+                                         int& b) {
+  const int G = gridDim.x;
+  const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  if (u >= n_units) return false;
+  major = u / hb;
+  h = (u % hb) % H;
+  b = (u % hb) / H;
+  return true;
+}
+
+// 32 fp32 S^T values (raw bits) of key row r at query columns col0.. : queries
+// before the key get -inf when the block is the diagonal one.
+__device__ __forceinline__ void mask_diag_t(uint32_t (&v)[32], int col0, int r) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (col0 + e < r) v[e] = 0xff800000u;
+}
+
+// Four 32-column TMEM loads of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld4x32(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3,
+                                            uint32_t (&a)[32], uint32_t (&b)[32],
+                                            uint32_t (&c)[32], uint32_t (&e)[32]) {
+  tmem_ld32_async(t0, a);
+  tmem_ld32_async(t1, b);
+  tmem_ld32_async(t2, c);
+  tmem_ld32_async(t3, e);
+  tmem_wait_regs(a);
+  reg_fence(b);
+  reg_fence(c);
+  reg_fence(e);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+  __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<uint32_t*>(&hv);
+}
+
+// ------------------------------------------------------------ dK / dV
+// Unit: key block jb; over the query blocks i = jb .. nqb-1 (keys are the M
+// dimension, so every product is a row-major one for this CTA's key rows):
+//   S^T = K Q_i^T, dP^T = V dO_i^T                      TMEM, fp32
+//   P^T = 2^(S^T/8 log2e - LSE_i log2e), dS^T = P^T (dP^T - D_i)  -> TMEM bf16
+//   dV += P^T dO_i, dK += dS^T Q_i                      TMEM, fp32
+// dK is scaled by 1/8 when it is written out.
+constexpr uint32_t DKV_S = 0, DKV_DP = 128, DKV_P = 256, DKV_DS = 320, DKV_DV = 384, DKV_DK = 448;
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_qkv,
-                     const __grid_constant__ CUtensorMap tm_do, const AttnArgs A) {
+                     const __grid_constant__ CUtensorMap tm_do, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sK = sm;
-  uint8_t* sV = sK + TILE;
-  uint8_t* sQ = sV + TILE;            // [2]
-  uint8_t* sdO = sQ + 2 * TILE;       // [2]
-  uint8_t* sPt = sdO + 2 * TILE;      // 32 KB
-  uint8_t* sdSt = sPt + PTILE;        // 32 KB
-  float* sL = reinterpret_cast<float*>(sdSt + PTILE);   // [2][128] LSE of the query block
-  float* sD = sL + 2 * AB;                               // [2][128] D of the query block
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sD + 2 * AB);
-  uint64_t *kv_full = bar, *in_full = bar + 1, *in_empty = bar + 3, *st_full = bar + 5,
-           *st_free = bar + 6, *ds_full = bar + 7, *acc_done = bar + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+  uint8_t* sK = sm;                          // [2 slots]
+  uint8_t* sV = sK + 2 * TILE;               // [2 slots]
+  uint8_t* sQ = sV + 2 * TILE;               // [BWD_NST]
+  uint8_t* sdO = sQ + BWD_NST * TILE;        // [BWD_NST]
+  float* sL = reinterpret_cast<float*>(sdO + BWD_NST * TILE);   // [BWD_NST][128] LSE
+  float* sD = sL + BWD_NST * AB;                                 // [BWD_NST][128] D
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sD + BWD_NST * AB);
+  uint64_t *kv_full = bar, *kv_empty = bar + 2, *in_full = bar + 4, *in_empty = in_full + BWD_NST;
+  uint64_t *st_full = in_empty + BWD_NST, *st_free = st_full + 1, *ds_full = st_full + 2,
+           *acc_done = st_full + 3, *o_free = st_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int nqb = A.S / AB;
-  const int jb = blockIdx.x;                       // key block; most work first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int n_it = nqb - jb;                       // query blocks jb .. nqb-1
+  const int hb = A.H * nb;
+  const int n_units = nqb * hb;
   const int d = A.H * AD;
-  const int row0 = b * A.S;
-  const size_t lrow = ((size_t)b * A.H + h) * A.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < BWD_NST; ++i) {
       mbar_init(&in_full[i], 1);
       mbar_init(&in_empty[i], 1);
     }
@@ -534,311 +557,446 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     mbar_init(st_free, NSWT);
     mbar_init(ds_full, NSWT);
     mbar_init(acc_done, 1);
+    mbar_init(o_free, NSWT);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  if (warp == 9) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tSt = *tmem_slot, tdPt = tSt + 128, tdV = tSt + 256, tdK = tSt + 320;
+  const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
-      auto load_in = [&](int t) {
-        const int i = jb + t, bf = t & 1;
-        mbar_expect_tx(&in_full[bf], 2 * TILE + 2 * AB * 4);
-        tma_load_2d(sQ + bf * TILE, &tm_qkv, &in_full[bf], h * AD, row0 + i * AB);
-        tma_load_2d(sdO + bf * TILE, &tm_do, &in_full[bf], h * AD, row0 + i * AB);
-        bulk_load(sL + bf * AB, A.lse + lrow + i * AB, AB * 4, &in_full[bf]);
-        bulk_load(sD + bf * AB, A.dsum + lrow + i * AB, AB * 4, &in_full[bf]);
-      };
-      auto mma_acc = [&](int t) -> bool {
-        if (!mbar_wait(ds_full, t & 1)) return false;
-        tc_fence_after();
-        const int bf = t & 1;
-#pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16(tdV, kdesc_p(sPt, kk), mndesc(sdO + bf * TILE, kk), IDESC_128x64_KMN, (t | kk) > 0);
-#pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16(tdK, kdesc_p(sdSt, kk), mndesc(sQ + bf * TILE, kk), IDESC_128x64_KMN, (t | kk) > 0);
-        mma_commit(acc_done);
-        mma_commit(&in_empty[bf]);
-        return true;
-      };
       bool ok = true;
-      mbar_expect_tx(kv_full, 2 * TILE);
-      tma_load_2d(sK, &tm_qkv, kv_full, d + h * AD, row0 + jb * AB);
-      tma_load_2d(sV, &tm_qkv, kv_full, 2 * d + h * AD, row0 + jb * AB);
-      load_in(0);
-      if (n_it > 1) load_in(1);
-      for (int t = 0; t < n_it && ok; ++t) {
-        ok = mbar_wait(&in_full[t & 1], (t >> 1) & 1) && (t > 0 || mbar_wait(kv_full, 0)) &&
-             (t == 0 || mbar_wait(st_free, (t - 1) & 1));
+      int g = 0, jb, h, b;
+      for (int k = 0; ok && bwd_unit(k, n_units, hb, A.H, jb, h, b); ++k) {
+        const int row0 = b * A.S, slot = k & 1, n = nqb - jb;
+        const size_t lrow = ((size_t)b * A.H + h) * A.S;
+        ok = mbar_wait(&kv_empty[slot], ((k >> 1) & 1) ^ 1);
         if (!ok) break;
-        tc_fence_after();
-        const uint8_t* q = sQ + (t & 1) * TILE;
-        const uint8_t* g = sdO + (t & 1) * TILE;
-#pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_bf16(tSt, kdesc(sK, kk), kdesc(q, kk), IDESC_128x128_KK, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_bf16(tdPt, kdesc(sV, kk), kdesc(g, kk), IDESC_128x128_KK, kk > 0);
-        mma_commit(st_full);
-        if (t > 0) ok = mma_acc(t - 1);
-        if (ok && t + 1 < n_it && t + 1 >= 2) {
-          ok = mbar_wait(&in_empty[(t + 1) & 1], ((t - 1) >> 1) & 1);
-          if (ok) load_in(t + 1);
+        mbar_expect_tx(&kv_full[slot], 2 * TILE);
+        tma_load_2d(sK + slot * TILE, &tm_qkv, &kv_full[slot], d + h * AD, row0 + jb * AB);
+        tma_load_2d(sV + slot * TILE, &tm_qkv, &kv_full[slot], 2 * d + h * AD, row0 + jb * AB);
+        for (int j = 0; j < n; ++j, ++g) {
+          const int i = jb + j, st = g % BWD_NST;
+          ok = mbar_wait(&in_empty[st], ((g / BWD_NST) & 1) ^ 1);
+          if (!ok) break;
+          mbar_expect_tx(&in_full[st], 2 * TILE + 2 * AB * 4);
+          tma_load_2d(sQ + st * TILE, &tm_qkv, &in_full[st], h * AD, row0 + i * AB);
+          tma_load_2d(sdO + st * TILE, &tm_do, &in_full[st], h * AD, row0 + i * AB);
+          bulk_load(sL + st * AB, A.lse + lrow + i * AB, AB * 4, &in_full[st]);
+          bulk_load(sD + st * AB, A.dsum + lrow + i * AB, AB * 4, &in_full[st]);
         }
       }
-      if (ok) ok = mma_acc(n_it - 1);
+      if (!ok) fail_wait(A.err, abort_flag);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint64_t TSTEP = TILE >> 4;
+      const uint64_t dk0 = kdesc(sK, 0), dv0 = kdesc(sV, 0), dq0 = kdesc(sQ, 0),
+                     ddo0 = kdesc(sdO, 0), mq0 = mndesc(sQ, 0), mdo0 = mndesc(sdO, 0);
+      struct Cursor {
+        int k, j, g, jb, h, b;
+        bool valid;
+      };
+      auto advance = [&](Cursor& c) {
+        ++c.g;
+        if (++c.j >= nqb - c.jb) {
+          c.j = 0;
+          ++c.k;
+          c.valid = bwd_unit(c.k, n_units, hb, A.H, c.jb, c.h, c.b);
+        }
+      };
+      Cursor ca;
+      ca.k = ca.j = ca.g = 0;
+      ca.valid = bwd_unit(0, n_units, hb, A.H, ca.jb, ca.h, ca.b);
+      Cursor cb = ca;
+      bool ok = true;
+      uint32_t idle = 0;
+      while (cb.valid) {
+        bool did = false;
+        if (ca.valid) {
+          const int st = ca.g % BWD_NST, slot = ca.k & 1;
+          if ((ca.j > 0 || mbar_test(&kv_full[slot], (ca.k >> 1) & 1)) &&
+              mbar_test(&in_full[st], (ca.g / BWD_NST) & 1) &&
+              (ca.g == 0 || mbar_test(st_free, (ca.g - 1) & 1))) {
+            tc_fence_after();
+            const uint64_t ak = dk0 + (uint64_t)slot * TSTEP, av = dv0 + (uint64_t)slot * TSTEP;
+            const uint64_t bq = dq0 + (uint64_t)st * TSTEP, bo = ddo0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AD / 16; ++kk)
+              mma_bf16(tbase + DKV_S, ak + kk * 2, bq + kk * 2, IDESC_128x128_KK, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < AD / 16; ++kk)
+              mma_bf16(tbase + DKV_DP, av + kk * 2, bo + kk * 2, IDESC_128x128_KK, kk > 0);
+            mma_commit(st_full);
+            if (ca.j == nqb - ca.jb - 1) mma_commit(&kv_empty[slot]);
+            advance(ca);
+            did = true;
+          }
+        }
+        if (cb.g < ca.g) {
+          // dV and dK overwrite their accumulators at a unit's first block:
+          // the previous unit's results are read out
+          if (mbar_test(ds_full, cb.g & 1) &&
+              (cb.j != 0 || cb.k == 0 || mbar_test(o_free, (cb.k - 1) & 1))) {
+            tc_fence_after();
+            const int st = cb.g % BWD_NST;
+            const uint64_t bo = mdo0 + (uint64_t)st * TSTEP, bq = mq0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AB / 16; ++kk)
+              mma_bf16_ts(tbase + DKV_DV, tbase + DKV_P + kk * 8, bo + kk * 128, IDESC_128x64_KMN,
+                          kk > 0 || cb.j > 0);
+#pragma unroll
+            for (int kk = 0; kk < AB / 16; ++kk)
+              mma_bf16_ts(tbase + DKV_DK, tbase + DKV_DS + kk * 8, bq + kk * 128, IDESC_128x64_KMN,
+                          kk > 0 || cb.j > 0);
+            mma_commit(acc_done);
+            mma_commit(&in_empty[st]);
+            advance(cb);
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          ok = false;
+          break;
+        }
+      }
       if (!ok) fail_wait(A.err, abort_flag);
     }
   } else {
+    // ---------------- elementwise: warps 0-7 ----------------
     const int quarter = warp & 3;
-    const int half = (warp - 1) >> 2;            // query columns half*64 .. +63
-    const int r = quarter * 32 + lane;
-    const int kj = jb * AB + r;                  // key position
+    const int half = warp >> 2;
+    const int r = quarter * 32 + lane;             // key row within the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tbase + DKV_S + 64 * half + lane_off;
+    const uint32_t tDP = tbase + DKV_DP + 64 * half + lane_off;
+    const uint32_t tP = tbase + DKV_P + 32 * half + lane_off;
+    const uint32_t tDS = tbase + DKV_DS + 32 * half + lane_off;
     const float scale2 = LOG2E * 0.125f;
+    const float2 sc2 = make_float2(scale2, scale2), nlog2 = make_float2(-LOG2E, -LOG2E);
     bool ok = true;
-    for (int t = 0; t < n_it; ++t) {
-      const int bf = t & 1;
-      if (!mbar_wait(st_full, t & 1) || !mbar_wait(&in_full[bf], (t >> 1) & 1) ||
-          (t > 0 && !mbar_wait(acc_done, (t - 1) & 1))) {
+    int g = 0, jb, h, b;
+    for (int k = 0; ok && bwd_unit(k, n_units, hb, A.H, jb, h, b); ++k) {
+      const int n = nqb - jb;
+      for (int j = 0; j < n; ++j, ++g) {
+        const int st = g % BWD_NST;
+        if (!mbar_wait(st_full, g & 1) || !mbar_wait(&in_full[st], (g / BWD_NST) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld4x32(tS, tS + 32, tDP, tDP + 32, sv[0], sv[1], dv[0], dv[1]);
+        tc_fence_before();
+        mbar_arrive(st_free);                      // S^T, dP^T may be overwritten
+        if (j == 0) {
+          mask_diag_t(sv[0], 64 * half, r);
+          mask_diag_t(sv[1], 64 * half + 32, r);
+        }
+        const float* L = sL + st * AB + 64 * half;
+        const float* Dv = sD + st * AB + 64 * half;
+        uint32_t pp[2][16], pd[2][16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = reinterpret_cast<const float4*>(L + 32 * c)[e4];
+            const float4 d4 = reinterpret_cast<const float4*>(Dv + 32 * c)[e4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const int e = e4 * 4 + u;
+              const float2 l2 = u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+              const float2 d2 = u ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+              const float2 y = __ffma2_rn(u2f2(sv[c][e], sv[c][e + 1]), sc2, __fmul2_rn(l2, nlog2));
+              const float2 p = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
+              const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[c][e], dv[c][e + 1]), d2));
+              pp[c][e >> 1] = pack_bf16(p.x, p.y);
+              pd[c][e >> 1] = pack_bf16(ds.x, ds.y);
+            }
+          }
+        }
+        // P^T and dS^T are free once the previous block's dV, dK products are done
+        if (g > 0 && !mbar_wait(acc_done, (g - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(tP, pp[0]);
+        tmem_st16(tP + 16, pp[1]);
+        tmem_st16(tDS, pd[0]);
+        tmem_st16(tDS + 16, pd[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      // unit end: dV and dK (x 1/8) of this CTA's key rows
+      if (!mbar_wait(acc_done, (g - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = (t == 0);                // query block jb holds the diagonal
-      const float* L = sL + bf * AB;
-      const float* Dv = sD + bf * AB;
-      const float2 sc2 = make_float2(scale2, scale2), nlog2 = make_float2(-LOG2E, -LOG2E);
-#pragma unroll 1
-      for (int c4 = 2 * half; c4 < 2 * half + 2; ++c4) {
-        uint32_t s[32], dp[32];
-        tmem_ld32_async(tSt + lane_off + c4 * 32, s);
-        tmem_ld32_async(tdPt + lane_off + c4 * 32, dp);
-        tmem_wait();
-        if (diag) {   // queries before the key get -inf, so their 2^x is 0
-          const int lim = r - c4 * 32;
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e < lim) s[e] = 0xff800000u;
-        }
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = reinterpret_cast<const float4*>(L + c4 * 32)[e4];
-          const float4 d4 = reinterpret_cast<const float4*>(Dv + c4 * 32)[e4];
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            const int e = e4 * 4 + u;
-            const float2 l2 = u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
-            const float2 d2 = u ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-            // p = 2^(s * log2(e) / 8 - LSE * log2(e)), dS = p (dP - D)
-            const float2 y = __ffma2_rn(u2f2(s[e], s[e + 1]), sc2, __fmul2_rn(l2, nlog2));
-            const float2 pp = make_float2(ex2(y.x), ex2(y.y));
-            const float2 ds = __fmul2_rn(pp, __fadd2_rn(u2f2(dp[e], dp[e + 1]), d2));
-            s[e] = __float_as_uint(pp.x);
-            s[e + 1] = __float_as_uint(pp.y);
-            dp[e] = __float_as_uint(ds.x);
-            dp[e + 1] = __float_as_uint(ds.y);
-          }
-        }
-        store_row_chunk_bits(sPt, r, c4 * 4, s);
-        store_row_chunk_bits(sdSt, r, c4 * 4, dp);
-      }
-      tc_fence_before();
-      mbar_arrive(st_free);
-      fence_proxy_async();
-      mbar_arrive(ds_full);
-    }
-    if (ok && mbar_wait(acc_done, (n_it - 1) & 1)) {
-      tc_fence_after();
-      bf16* outk = A.dqkv + (size_t)(row0 + kj) * 3 * d + d + h * AD + half * 32;
-      bf16* outv = A.dqkv + (size_t)(row0 + kj) * 3 * d + 2 * d + h * AD + half * 32;
+      const size_t row = (size_t)(b * A.S + jb * AB + r) * 3 * d;
       float v[32];
-      tmem_ld32(tdV + lane_off + half * 32, v);
-      store8_bf16_row(outv, v, 1.0f);
-      tmem_ld32(tdK + lane_off + half * 32, v);
-      store8_bf16_row(outk, v, 0.125f);
-    } else {
-      fail_wait(A.err, abort_flag);
+      tmem_ld32(tbase + DKV_DV + 32 * half + lane_off, v);
+      store8_bf16_row(A.dqkv + row + 2 * d + h * AD + 32 * half, v, 1.0f);
+      tmem_ld32(tbase + DKV_DK + 32 * half + lane_off, v);
+      store8_bf16_row(A.dqkv + row + d + h * AD + 32 * half, v, 0.125f);
+      tc_fence_before();
+      mbar_arrive(o_free);
     }
+    if (!ok) fail_wait(A.err, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(*tmem_slot, 512);
+    tmem_dealloc(tbase, 512);
   }
 }
 
-// ============================================================ backward dQ
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// ------------------------------------------------------------ dQ
+// Unit: query block ib; over the key blocks j = 0 .. ib:
+//   S = Q K_j^T, dP = dO V_j^T                          TMEM, fp32
+//   dS = 2^(S/8 log2e - LSE log2e) (dP - D)             -> TMEM bf16, two buffers
+//   dQ += dS K_j                                        TMEM, fp32
+// dQ is scaled by 1/8 when it is written out.
+constexpr uint32_t DQ_S = 0, DQ_DP = 128, DQ_DS = 256, DQ_DQ = 384;
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_qkv,
-                   const __grid_constant__ CUtensorMap tm_do, const AttnArgs A) {
+                   const __grid_constant__ CUtensorMap tm_do, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sQ = sm;
-  uint8_t* sdO = sQ + TILE;
-  uint8_t* sK = sdO + TILE;           // [2]
-  uint8_t* sV = sK + 2 * TILE;        // [2]
-  uint8_t* sdS = sV + 2 * TILE;       // 32 KB
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sdS + PTILE);
-  uint64_t *q_full = bar, *kv_full = bar + 1, *kv_empty = bar + 3, *s_full = bar + 5,
-           *s_free = bar + 6, *ds_full = bar + 7, *acc_done = bar + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+  uint8_t* sQ = sm;                          // [2 slots]
+  uint8_t* sdO = sQ + 2 * TILE;              // [2 slots]
+  uint8_t* sK = sdO + 2 * TILE;              // [BWD_NST]
+  uint8_t* sV = sK + BWD_NST * TILE;         // [BWD_NST]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sV + BWD_NST * TILE);
+  uint64_t *qd_full = bar, *qd_empty = bar + 2, *kv_full = bar + 4, *kv_empty = kv_full + BWD_NST;
+  uint64_t *s_full = kv_empty + BWD_NST, *s_free = s_full + 1, *ds_full = s_full + 2,
+           *dq_done = s_full + 4, *o_free = s_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int nqb = A.S / AB;
-  const int ib = nqb - 1 - blockIdx.x;             // most work first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int n_it = ib + 1;                         // key blocks 0 .. ib
+  const int hb = A.H * nb;
+  const int n_units = nqb * hb;
   const int d = A.H * AD;
-  const int row0 = b * A.S;
-  const size_t lrow = ((size_t)b * A.H + h) * A.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+      mbar_init(&ds_full[i], NSWT);
+      mbar_init(&dq_done[i], 1);
+    }
+    for (int i = 0; i < BWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, NSWT);
-    mbar_init(ds_full, NSWT);
-    mbar_init(acc_done, 1);
+    mbar_init(o_free, NSWT);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  if (warp == 9) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = *tmem_slot, tdP = tS + 128, tdQ = tS + 256;
+  const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
-      auto load_kv = [&](int t) {
-        const int bf = t & 1;
-        mbar_expect_tx(&kv_full[bf], 2 * TILE);
-        tma_load_2d(sK + bf * TILE, &tm_qkv, &kv_full[bf], d + h * AD, row0 + t * AB);
-        tma_load_2d(sV + bf * TILE, &tm_qkv, &kv_full[bf], 2 * d + h * AD, row0 + t * AB);
-      };
-      auto mma_acc = [&](int t) -> bool {
-        if (!mbar_wait(ds_full, t & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16(tdQ, kdesc_p(sdS, kk), mndesc(sK + (t & 1) * TILE, kk), IDESC_128x64_KMN,
-                   (t | kk) > 0);
-        mma_commit(acc_done);
-        mma_commit(&kv_empty[t & 1]);
-        return true;
-      };
       bool ok = true;
-      mbar_expect_tx(q_full, 2 * TILE);
-      tma_load_2d(sQ, &tm_qkv, q_full, h * AD, row0 + ib * AB);
-      tma_load_2d(sdO, &tm_do, q_full, h * AD, row0 + ib * AB);
-      load_kv(0);
-      if (n_it > 1) load_kv(1);
-      for (int t = 0; t < n_it && ok; ++t) {
-        ok = mbar_wait(&kv_full[t & 1], (t >> 1) & 1) && (t > 0 || mbar_wait(q_full, 0)) &&
-             (t == 0 || mbar_wait(s_free, (t - 1) & 1));
+      int g = 0, mj, h, b;
+      for (int k = 0; ok && bwd_unit(k, n_units, hb, A.H, mj, h, b); ++k) {
+        const int ib = nqb - 1 - mj, row0 = b * A.S, slot = k & 1;
+        ok = mbar_wait(&qd_empty[slot], ((k >> 1) & 1) ^ 1);
         if (!ok) break;
-        tc_fence_after();
-        const uint8_t* k = sK + (t & 1) * TILE;
-        const uint8_t* v = sV + (t & 1) * TILE;
-#pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_bf16(tS, kdesc(sQ, kk), kdesc(k, kk), IDESC_128x128_KK, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_bf16(tdP, kdesc(sdO, kk), kdesc(v, kk), IDESC_128x128_KK, kk > 0);
-        mma_commit(s_full);
-        if (t > 0) ok = mma_acc(t - 1);
-        if (ok && t + 1 < n_it && t + 1 >= 2) {
-          ok = mbar_wait(&kv_empty[(t + 1) & 1], ((t - 1) >> 1) & 1);
-          if (ok) load_kv(t + 1);
+        mbar_expect_tx(&qd_full[slot], 2 * TILE);
+        tma_load_2d(sQ + slot * TILE, &tm_qkv, &qd_full[slot], h * AD, row0 + ib * AB);
+        tma_load_2d(sdO + slot * TILE, &tm_do, &qd_full[slot], h * AD, row0 + ib * AB);
+        for (int j = 0; j <= ib; ++j, ++g) {
+          const int st = g % BWD_NST;
+          ok = mbar_wait(&kv_empty[st], ((g / BWD_NST) & 1) ^ 1);
+          if (!ok) break;
+          mbar_expect_tx(&kv_full[st], 2 * TILE);
+          tma_load_2d(sK + st * TILE, &tm_qkv, &kv_full[st], d + h * AD, row0 + j * AB);
+          tma_load_2d(sV + st * TILE, &tm_qkv, &kv_full[st], 2 * d + h * AD, row0 + j * AB);
         }
       }
-      if (ok) ok = mma_acc(n_it - 1);
+      if (!ok) fail_wait(A.err, abort_flag);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint64_t TSTEP = TILE >> 4;
+      const uint64_t dq0 = kdesc(sQ, 0), ddo0 = kdesc(sdO, 0), dk0 = kdesc(sK, 0),
+                     dv0 = kdesc(sV, 0), mk0 = mndesc(sK, 0);
+      struct Cursor {
+        int k, j, g, ib, h, b;
+        bool valid;
+      };
+      auto load_unit = [&](Cursor& c) {
+        int mj;
+        c.valid = bwd_unit(c.k, n_units, hb, A.H, mj, c.h, c.b);
+        c.ib = nqb - 1 - mj;
+      };
+      auto advance = [&](Cursor& c) {
+        ++c.g;
+        if (++c.j > c.ib) {
+          c.j = 0;
+          ++c.k;
+          load_unit(c);
+        }
+      };
+      Cursor ca;
+      ca.k = ca.j = ca.g = 0;
+      load_unit(ca);
+      Cursor cb = ca;
+      bool ok = true;
+      uint32_t idle = 0;
+      while (cb.valid) {
+        bool did = false;
+        if (ca.valid) {
+          const int st = ca.g % BWD_NST, slot = ca.k & 1;
+          if ((ca.j > 0 || mbar_test(&qd_full[slot], (ca.k >> 1) & 1)) &&
+              mbar_test(&kv_full[st], (ca.g / BWD_NST) & 1) &&
+              (ca.g == 0 || mbar_test(s_free, (ca.g - 1) & 1))) {
+            tc_fence_after();
+            const uint64_t aq = dq0 + (uint64_t)slot * TSTEP, ao = ddo0 + (uint64_t)slot * TSTEP;
+            const uint64_t bk = dk0 + (uint64_t)st * TSTEP, bv = dv0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AD / 16; ++kk)
+              mma_bf16(tbase + DQ_S, aq + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < AD / 16; ++kk)
+              mma_bf16(tbase + DQ_DP, ao + kk * 2, bv + kk * 2, IDESC_128x128_KK, kk > 0);
+            mma_commit(s_full);
+            if (ca.j == ca.ib) mma_commit(&qd_empty[slot]);
+            advance(ca);
+            did = true;
+          }
+        }
+        if (cb.g < ca.g) {
+          const int pb = cb.g & 1;
+          // dQ is overwritten at a unit's first block: the previous unit's dQ is read out
+          if (mbar_test(&ds_full[pb], (cb.g >> 1) & 1) &&
+              (cb.j != 0 || cb.k == 0 || mbar_test(o_free, (cb.k - 1) & 1))) {
+            tc_fence_after();
+            const int st = cb.g % BWD_NST;
+            const uint64_t bk = mk0 + (uint64_t)st * TSTEP;
+#pragma unroll
+            for (int kk = 0; kk < AB / 16; ++kk)
+              mma_bf16_ts(tbase + DQ_DQ, tbase + DQ_DS + 64 * pb + kk * 8, bk + kk * 128,
+                          IDESC_128x64_KMN, kk > 0 || cb.j > 0);
+            mma_commit(&dq_done[pb]);
+            mma_commit(&kv_empty[st]);
+            advance(cb);
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          ok = false;
+          break;
+        }
+      }
       if (!ok) fail_wait(A.err, abort_flag);
     }
   } else {
+    // ---------------- elementwise: warps 0-7 ----------------
     const int quarter = warp & 3;
-    const int half = (warp - 1) >> 2;            // key columns half*64 .. +63
-    const int r = quarter * 32 + lane;
-    const int qi = ib * AB + r;
+    const int half = warp >> 2;
+    const int r = quarter * 32 + lane;             // query row within the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tbase + DQ_S + 64 * half + lane_off;
+    const uint32_t tDP = tbase + DQ_DP + 64 * half + lane_off;
+    const uint32_t tDS = tbase + DQ_DS + 32 * half + lane_off;
     const float scale2 = LOG2E * 0.125f;
-    const float L2 = A.lse[lrow + qi] * LOG2E;
-    const float Di = A.dsum[lrow + qi];
+    const float2 sc2 = make_float2(scale2, scale2);
     bool ok = true;
-    for (int t = 0; t < n_it; ++t) {
-      if (!mbar_wait(s_full, t & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32_async(tS + lane_off + half * 64, sr[0]);
-      tmem_ld32_async(tS + lane_off + half * 64 + 32, sr[1]);
-      tmem_ld32_async(tdP + lane_off + half * 64, dr[0]);
-      tmem_ld32_async(tdP + lane_off + half * 64 + 32, dr[1]);
-      tmem_wait();
-      tc_fence_before();
-      mbar_arrive(s_free);                         // S, dP are in registers
-      if (t > 0 && !mbar_wait(acc_done, (t - 1) & 1)) {   // dS tile free again
-        ok = false;
-        break;
-      }
-      if (t == ib) {   // keys after the query get -inf, so their 2^x is 0
-        const int lim = r - half * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e > lim) sr[c][e] = 0xff800000u;
-      }
-      // p = 2^(s * log2(e) / 8 - LSE * log2(e)), dS = p (dP - D), two lanes at a time
-      const float2 sc2 = make_float2(scale2, scale2), nl2 = make_float2(-L2, -L2),
-                   nd2 = make_float2(-Di, -Di);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 y = __ffma2_rn(u2f2(sr[c][e], sr[c][e + 1]), sc2, nl2);
-          const float2 pp = make_float2(ex2(y.x), ex2(y.y));
-          const float2 ds = __fmul2_rn(pp, __fadd2_rn(u2f2(dr[c][e], dr[c][e + 1]), nd2));
-          dr[c][e] = __float_as_uint(ds.x);
-          dr[c][e + 1] = __float_as_uint(ds.y);
+    int g = 0, mj, h, b;
+    for (int k = 0; ok && bwd_unit(k, n_units, hb, A.H, mj, h, b); ++k) {
+      const int ib = nqb - 1 - mj;
+      const size_t lrow = ((size_t)b * A.H + h) * A.S + ib * AB + r;
+      const float L2 = A.lse[lrow] * LOG2E, Di = A.dsum[lrow];
+      const float2 nl2 = make_float2(-L2, -L2), nd2 = make_float2(-Di, -Di);
+      for (int j = 0; j <= ib; ++j, ++g) {
+        if (!mbar_wait(s_full, g & 1)) {
+          ok = false;
+          break;
         }
-        store_row_chunk_bits(sdS, r, (half * 2 + c) * 4, dr[c]);
+        tc_fence_after();
+        uint32_t sv[2][32], dv[2][32];
+        tmem_ld4x32(tS, tS + 32, tDP, tDP + 32, sv[0], sv[1], dv[0], dv[1]);
+        tc_fence_before();
+        mbar_arrive(s_free);                       // S, dP may be overwritten
+        if (j == ib) {
+          mask_diag(sv[0], 64 * half, r);
+          mask_diag(sv[1], 64 * half + 32, r);
+        }
+        uint32_t pd[2][16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 y = __ffma2_rn(u2f2(sv[c][e], sv[c][e + 1]), sc2, nl2);
+            const float2 p = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
+            const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[c][e], dv[c][e + 1]), nd2));
+            pd[c][e >> 1] = pack_bf16(ds.x, ds.y);
+          }
+        }
+        // dS[g & 1] was read by the dQ product of block g-2
+        const int pb = g & 1;
+        if (g >= 2 && !mbar_wait(&dq_done[pb], ((g - 2) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(tDS + 64 * pb, pd[0]);
+        tmem_st16(tDS + 64 * pb + 16, pd[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ds_full[pb]);
       }
-      fence_proxy_async();
-      mbar_arrive(ds_full);
-    }
-    if (ok && mbar_wait(acc_done, (n_it - 1) & 1)) {
+      if (!ok) break;
+      // unit end: dQ x 1/8 of this CTA's query rows
+      const int gl = g - 1;
+      if (!mbar_wait(&dq_done[gl & 1], (gl >> 1) & 1)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       float v[32];
-      tmem_ld32(tdQ + lane_off + half * 32, v);
-      store8_bf16_row(A.dqkv + (size_t)(row0 + qi) * 3 * d + h * AD + half * 32, v, 0.125f);
-    } else {
-      fail_wait(A.err, abort_flag);
+      tmem_ld32(tbase + DQ_DQ + 32 * half + lane_off, v);
+      store8_bf16_row(A.dqkv + (size_t)(b * A.S + ib * AB + r) * 3 * d + h * AD + 32 * half, v,
+                      0.125f);
+      tc_fence_before();
+      mbar_arrive(o_free);
     }
+    if (!ok) fail_wait(A.err, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(*tmem_slot, 512);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -875,8 +1033,8 @@ bool map_128x64(CUtensorMap* m, const void* base, long long rows, long long cols
 }
 
 constexpr size_t SMEM_FWD = 1024 + TILE * (2 + 2 * FWD_NST) + 256 + 4 * AB * 4;
-constexpr size_t SMEM_DKDV = 1024 + TILE * 6 + 2 * PTILE + 4 * AB * 4 + 128;
-constexpr size_t SMEM_DQ = 1024 + TILE * 6 + PTILE + 128;
+constexpr size_t SMEM_DKDV = 1024 + TILE * (4 + 2 * BWD_NST) + 2 * BWD_NST * AB * 4 + 256;
+constexpr size_t SMEM_DQ = 1024 + TILE * (4 + 2 * BWD_NST) + 256;
 
 template <typename K>
 cudaError_t set_smem(K kern, size_t bytes) {
@@ -924,8 +1082,13 @@ cudaError_t attn_bwd_tc_launch(const void* qkv, const void* dout, const float* l
       !map_128x64(&mo, dout, (long long)nb * S, (long long)H * AD, (long long)H * AD))
     return cudaErrorInvalidValue;
   AttnArgs a{S, H, nullptr, const_cast<float*>(lse), dsum, (bf16*)dqkv, err};
-  attn_bwd_dkdv_tc<<<dim3(S / AB, H, nb), AT_THREADS, SMEM_DKDV, s>>>(mq, mo, a);
-  attn_bwd_dq_tc<<<dim3(S / AB, H, nb), AT_THREADS, SMEM_DQ, s>>>(mq, mo, a);
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int units = (S / AB) * H * nb;
+  const int grid = units < sms ? units : sms;
+  attn_bwd_dkdv_tc<<<grid, BWD_THREADS, SMEM_DKDV, s>>>(mq, mo, a, nb);
+  attn_bwd_dq_tc<<<grid, BWD_THREADS, SMEM_DQ, s>>>(mq, mo, a, nb);
   return cudaGetLastError();
 }
 
