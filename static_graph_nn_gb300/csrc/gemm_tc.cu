@@ -37,6 +37,7 @@ constexpr int TC_THREADS = 320;          // warp 0 TMA, warp 1 MMA, warps 2-9 ep
 struct TcParams {
   GemmArgs g;
   int tiles_m, tiles_n, k_blocks;
+  int splits, kb_per;                  // split-K: K blocks [s*kb_per, (s+1)*kb_per) per split
   int vec;                             // epilogue pointers/strides allow 16-byte vectors
   int* err;                            // set to 1 on a timed-out wait
 };
@@ -149,6 +150,24 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int 
   }
 }
 
+// Split-K partial sum of 32 consecutive fp32 columns of one row, added into
+// the (zeroed) output with vector atomics.  Used only for plain fp32 outputs
+// (weight gradients: no bias, activation or residual in the epilogue).
+__device__ __forceinline__ void split_add_row32(const GemmArgs& g, bool vec, int m, int n0,
+                                                const float (&v)[32]) {
+  float* out = static_cast<float*>(g.out) + (size_t)m * g.ldo + n0;
+  if (vec && n0 + 32 <= g.N) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      atomicAdd(reinterpret_cast<float4*>(out) + q,
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (n0 + j < g.N) atomicAdd(out + j, v[j]);
+}
+
 template <int BN, int STAGES, typename TO, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -170,7 +189,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = P.tiles_m * P.tiles_n;
+  const int n_items = P.tiles_m * P.tiles_n * P.splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -202,9 +221,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+        const int tile = item / P.splits, sp = item % P.splits;
         const int m0 = (tile / P.tiles_n) * TC_BM, n0 = (tile % P.tiles_n) * BN;
-        for (int kb = 0; kb < P.k_blocks; ++kb) {
+        const int kb0 = sp * P.kb_per, kb1 = min(P.k_blocks, kb0 + P.kb_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
           mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
           const int k0 = kb * TC_BK;
@@ -233,14 +254,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++it) {
+        const int sp = item % P.splits;
+        const int kb0 = sp * P.kb_per, kb1 = min(P.k_blocks, kb0 + P.kb_per);
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(&tempty[acc], use ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < P.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a = smem_u32(sA + stage * A_BYTES);
@@ -251,7 +274,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                      : smem_desc(a + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(b + k * 2048, 64 * TC_BK * 2, 1024)
                                      : smem_desc(b + k * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb | k) ? 1u : 0u);
+            mma_bf16(d, ad, bd, idesc, (kb > kb0 || k) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);           // frees the stage when these MMAs finish
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -266,7 +289,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int half = (warp - 2) >> 2;          // columns half*BN/2 .. (half+1)*BN/2-1
     const int row_in_tile = quarter * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+      const int tile = item / P.splits;
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], use)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
@@ -279,7 +303,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        if (m < P.g.M && n0 + c * 32 < P.g.N) epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+        if (m < P.g.M && n0 + c * 32 < P.g.N) {
+          if (P.splits > 1)
+            split_add_row32(P.g, P.vec != 0, m, n0 + c * 32, v);
+          else
+            epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -357,6 +386,8 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
   P.tiles_m = (g.M + TC_BM - 1) / TC_BM;
   P.tiles_n = (g.N + BN - 1) / BN;
   P.k_blocks = (g.K + TC_BK - 1) / TC_BK;
+  P.splits = 1;
+  P.kb_per = P.k_blocks;
   P.err = err;
   {
     auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -373,7 +404,30 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
     attr_set = true;
   }
   const int tiles = P.tiles_m * P.tiles_n;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  // Split-K for plain fp32 outputs (weight gradients) when the tiles leave
+  // SMs idle: the split count that minimises rounds of work / splits, with at
+  // least 4 K blocks per split; the partial sums are added into a zeroed output.
+  const bool plain = sizeof(TO) == 4 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  if (plain && tiles < num_sms()) {
+    double best = 1.0;
+    for (int sp = 2; sp <= 8 && P.k_blocks / sp >= 4; ++sp) {
+      const double cost = (double)((tiles * sp + num_sms() - 1) / num_sms()) / sp + 0.02 * sp;
+      if (cost < best - 1e-9) {
+        best = cost;
+        P.splits = sp;
+      }
+    }
+    if (P.splits > 1) {
+      P.kb_per = (P.k_blocks + P.splits - 1) / P.splits;
+      P.splits = (P.k_blocks + P.kb_per - 1) / P.kb_per;
+      cudaError_t e = g.ldo == g.N
+                          ? cudaMemsetAsync(g.out, 0, (size_t)g.M * g.N * 4, s)
+                          : cudaMemset2DAsync(g.out, (size_t)g.ldo * 4, 0, (size_t)g.N * 4, g.M, s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const int items = tiles * P.splits;
+  const int grid = items < num_sms() ? items : num_sms();
   kern<<<grid, TC_THREADS, smem, s>>>(ma, mb, P);
   return cudaGetLastError();
 }

@@ -56,7 +56,10 @@ cudaError_t mse_loss(DType t, const void* o, const void* target, size_t n, void*
 // ---- reductions / norms ----------------------------------------------------
 // out[n] = sum over rows of src[r, n]  (fp32 result), deterministic two passes.
 cudaError_t colsum(DType t, const void* src, int rows, int cols, long long ld, float* partials,
-                   int row_chunks, float* out, cudaStream_t s);
+                   size_t partial_floats, float* out, cudaStream_t s);
+// Target block count of colsum's first pass (about two per SM); a partials
+// buffer of kColsumBlocks * 2048 floats lets it reach that for any width.
+constexpr int kColsumBlocks = 2 * 152;
 cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, float* rstd, int rows,
                         int d, float eps, cudaStream_t s);
 // dx = r (g - x r^2 mean(g x)) + dadd, g = dy * gamma;  dgamma partial sums of dy * x * r.

@@ -35,9 +35,9 @@ std::string g_err = "";
 constexpr size_t kAlignElems = 64;      // parameter offsets (256 B in fp32)
 constexpr size_t kWsAlign = 1024;       // workspace region alignment
 constexpr int kChunk = 16384;           // optimizer chunk (elements)
-constexpr int kRowChunks = 64;          // column-sum partial rows
 constexpr int kNormChunks = 4 * 152;    // RMSNorm backward blocks (dgamma partial rows)
 constexpr int kMsePartials = 1024;
+constexpr size_t kColsumFloats = (size_t)kColsumBlocks * 2048;   // column-sum partials capacity
 
 enum NodeKind { NK_LINEAR, NK_RMSNORM, NK_ATTN };
 
@@ -101,7 +101,7 @@ struct mg_plan {
   size_t ws_bytes = 0;
   char* ws = nullptr;
   size_t shadow_off = 0, chunks_off = 0, loss_off = 0, rowloss_off = 0, partial_off = 0,
-         flag_off = 0;
+         colsum_off = 0, flag_off = 0;
   int n_chunks = 0;
   const float* last_params = nullptr;
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
@@ -339,8 +339,8 @@ void node_update(Exec& e, int ni) {
   const Chunk* chunks = wsp<Chunk>(p, p->chunks_off) + c0;
   void* shadow = p->dt == DT_BF16 ? p->ws + p->shadow_off : nullptr;
   if (!e.dry && e.err == cudaSuccess) {
-    cudaError_t r = cudaEventRecord(p->node_ev[ni], e.s);
-    if (r == cudaSuccess) r = cudaStreamWaitEvent(p->aux, p->node_ev[ni], 0);
+    cudaError_t r = cudaEventRecord(p->node_ev[2 * ni], e.s);
+    if (r == cudaSuccess) r = cudaStreamWaitEvent(p->aux, p->node_ev[2 * ni], 0);
     if (r != cudaSuccess) e.err = r;
   }
   char nm[96];
@@ -379,16 +379,24 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
       g.B = gy; g.ldb = n.d_out; g.b_k = 0;
       g.in_type = dt; g.aux_type = dt;
       g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
-      site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
-           [&] { return run_gemm(p, g, e.s); });
       if (n.has_bias) {
+        // db = column sums of dZ, on the auxiliary stream (only the optimizer
+        // reads it), overlapping this node's dW and dX products
+        if (!e.dry && e.err == cudaSuccess) {
+          cudaError_t r = cudaEventRecord(p->node_ev[2 * ni + 1], e.s);
+          if (r == cudaSuccess) r = cudaStreamWaitEvent(p->aux, p->node_ev[2 * ni + 1], 0);
+          if (r != cudaSuccess) e.err = r;
+        }
         char nm[96];
         snprintf(nm, sizeof nm, "db_colsum[l%d] %dx%d", n.layer, p->batch, n.d_out);
-        site(e, nm, 0, (double)dtype_size(dt) * p->batch * n.d_out + 4.0 * n.d_out, 2, [&] {
-          return colsum(dt, gy, p->batch, n.d_out, n.d_out, wsp<float>(p, p->partial_off),
-                        kRowChunks, grads + n.b_off, e.s);
-        });
+        site_on(e, p->aux, nm, 0, (double)dtype_size(dt) * p->batch * n.d_out + 4.0 * n.d_out, 2,
+                [&] {
+                  return colsum(dt, gy, p->batch, n.d_out, n.d_out, wsp<float>(p, p->colsum_off),
+                                kColsumFloats, grads + n.b_off, p->aux);
+                });
       }
+      site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+           [&] { return run_gemm(p, g, e.s); });
       if (vin.need_grad) {
         // dX = dZ W^T, times act'(saved) of the producer of X, plus the skip gradient
         GemmArgs h;
@@ -684,13 +692,12 @@ void layout_workspace(mg_plan* p) {
   p->loss_off = b.take(16);
   p->flag_off = b.take(16);
   p->rowloss_off = b.take(B * 4);
-  size_t maxw = 0;
-  for (auto& v : p->values) maxw = v.width > (int)maxw ? v.width : maxw;
-  size_t part = (size_t)kRowChunks * maxw * 4;
+  size_t part = 0;
   for (auto& n : p->nodes)
     if (n.kind == NK_RMSNORM && (size_t)kNormChunks * n.d * 4 > part) part = (size_t)kNormChunks * n.d * 4;
   if (part < (size_t)kMsePartials * 4) part = (size_t)kMsePartials * 4;
   p->partial_off = b.take(part);
+  p->colsum_off = b.take(kColsumFloats * 4);   // the bias-gradient sums' own partials (aux stream)
   p->ws_bytes = round_up(b.top, kWsAlign);
 }
 
@@ -793,7 +800,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
   e = cudaMemcpy(p->ws + p->chunks_off, ch.data(), ch.size() * sizeof(Chunk), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->ws + p->loss_off, 0, 16);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking);
-  p->node_ev.assign(p->nodes.size(), nullptr);
+  p->node_ev.assign(2 * p->nodes.size(), nullptr);   // per node: updates, bias-gradient sum
   for (auto& ev : p->node_ev)
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming);
