@@ -25,6 +25,12 @@ where the pages are silent:
 * Backward: the chain rule applied layer by layer in reverse.
 * SGD: p -= lr g.  Adam (t = step, from 1): bias-corrected moments, eps added
   after the square root, no weight decay.
+* LaProp (named beside Adam in the paper's checkpoint notes; its update is the
+  published algorithm of Ziyin, Wang & Ueda, "LaProp: Separating Momentum and
+  Adaptivity in Adam", 2020): the gradient is divided by the bias-corrected
+  root of its second moment before it enters the momentum.
+* SGD with momentum (heavy ball, no dampening): b = mu b + g, p -= lr b, with
+  mu in the descriptor's beta1.
 
 Precision: float64 arithmetic throughout, with the storage types of the typed
 static graph.  Three modes:
@@ -328,6 +334,30 @@ def adam_update(p, g, m, v, lr, step, beta1, beta2, eps):
     return p2.astype(np.float32), m2.astype(np.float32), v2.astype(np.float32)
 
 
+def laprop_update(p, g, m, v, lr, step, beta1, beta2, eps):
+    """One LaProp step, t = step (1-based), in the published algorithm's order:
+    v = b2 v + (1-b2) g^2; the gradient divided by sqrt(v / (1 - b2^t)) + eps
+    enters the momentum m = b1 m + (1-b1) (that quotient); p -= lr m /
+    (1 - b1^t).  Returns float32 (p, m, v)."""
+    v2 = beta2 * np.asarray(v, np.float64) + (1.0 - beta2) * g * g
+    vhat = v2 / (1.0 - beta2 ** step)
+    m2 = beta1 * np.asarray(m, np.float64) + (1.0 - beta1) * g / (np.sqrt(vhat) + eps)
+    p2 = np.asarray(p, np.float64) - lr * m2 / (1.0 - beta1 ** step)
+    return p2.astype(np.float32), m2.astype(np.float32), v2.astype(np.float32)
+
+
+def sgd_momentum_update(p, g, b, lr, mu):
+    """Heavy-ball SGD: b = mu b + g, p -= lr b.  Returns float32 (p, b)."""
+    b2 = mu * np.asarray(b, np.float64) + g
+    p2 = np.asarray(p, np.float64) - lr * b2
+    return p2.astype(np.float32), b2.astype(np.float32)
+
+
+# optimizer name -> moments it keeps: (first, second)
+MOMENTS = {"sgd": (False, False), "adam": (True, True), "laprop": (True, True),
+           "sgd_momentum": (True, False)}
+
+
 # --------------------------------------------------------------------------
 # One full training step
 # --------------------------------------------------------------------------
@@ -344,11 +374,16 @@ def train_step(layers, params, x, labels, loss_kind, precision, optimizer, lr, s
     for i, (p, g) in enumerate(zip(params, grads)):
         if optimizer == "sgd":
             new_p.append(sgd_update(p, g, lr))
-        elif optimizer == "adam":
-            a, b, c = adam_update(p, g, adam_m[i], adam_v[i], lr, step, beta1, beta2, eps)
+        elif optimizer in ("adam", "laprop"):
+            upd = adam_update if optimizer == "adam" else laprop_update
+            a, b, c = upd(p, g, adam_m[i], adam_v[i], lr, step, beta1, beta2, eps)
             new_p.append(a)
             new_m.append(b)
             new_v.append(c)
+        elif optimizer == "sgd_momentum":
+            a, b = sgd_momentum_update(p, g, adam_m[i], lr, beta1)
+            new_p.append(a)
+            new_m.append(b)
         else:
             raise ValueError(optimizer)
     return {"loss": loss, "out": out, "grads": grads, "params": new_p,
@@ -359,14 +394,17 @@ def run_steps(layers, params, x, labels, loss_kind, precision, optimizer, lr, n_
               beta1=0.9, beta2=0.999, eps=1e-8):
     """n_steps steps on one fixed batch; returns the per-step results."""
     p = [np.asarray(a, np.float32).copy() for a in params]
-    m = [np.zeros_like(a) for a in p] if optimizer == "adam" else None
-    v = [np.zeros_like(a) for a in p] if optimizer == "adam" else None
+    has_m, has_v = MOMENTS[optimizer]
+    m = [np.zeros_like(a) for a in p] if has_m else None
+    v = [np.zeros_like(a) for a in p] if has_v else None
     hist = []
     for t in range(1, n_steps + 1):
         r = train_step(layers, p, x, labels, loss_kind, precision, optimizer, lr, t,
                        m, v, beta1, beta2, eps)
         p = r["params"]
-        if optimizer == "adam":
-            m, v = r["adam_m"], r["adam_v"]
+        if has_m:
+            m = r["adam_m"]
+        if has_v:
+            v = r["adam_v"]
         hist.append(r)
     return hist

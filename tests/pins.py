@@ -148,6 +148,90 @@ def sgd_error():
     return float(np.abs(oracle.sgd_update(p, g, 0.1) - np.array([0.95, -2.025, 0.6])).max())
 
 
+def laprop_t1_error(seed=4):
+    """At t = 1 LaProp's second moment is (1-b2) g^2, whose bias-corrected root
+    is |g|; the momentum holds (1-b1) g/(|g|+eps), and dividing by (1-b1)
+    moves p by lr * g / (|g| + eps): a sign step of size lr."""
+    r = _rng(seed)
+    p = r.standard_normal(40).astype(np.float32)
+    g = r.standard_normal(40) * 10 ** r.uniform(-4, 1, 40)
+    lr, eps = 1e-3, 1e-8
+    p2, m2, v2 = oracle.laprop_update(p, g, np.zeros(40, np.float32), np.zeros(40, np.float32),
+                                      lr, 1, 0.9, 0.999, eps)
+    want = (p.astype(np.float64) - lr * g / (np.abs(g) + eps)).astype(np.float32)
+    e1 = np.abs(p2.astype(np.float64) - want).max()
+    e2 = np.abs(m2 - (0.1 * g / (np.abs(g) + eps)).astype(np.float32)).max()
+    e3 = np.abs(v2 - (0.001 * g * g).astype(np.float32)).max() / max(np.abs(v2).max(), 1e-30)
+    return float(max(e1, e2, e3))
+
+
+def laprop_constant_gradient_error():
+    """With the same gradient every step both bias corrections are exact, so
+    every step of LaProp moves p by lr * g / (|g| + eps): after five steps
+    p5 = p0 - 5 lr g / (|g| + eps)."""
+    lr, eps = 1e-2, 1e-8
+    g = np.array([0.3, -2.0, 1e-3])
+    p = np.array([1.0, 0.0, -1.0], np.float32)
+    m = np.zeros(3, np.float32)
+    v = np.zeros(3, np.float32)
+    for t in range(1, 6):
+        p, m, v = oracle.laprop_update(p, g, m, v, lr, t, 0.9, 0.999, eps)
+    want = np.array([1.0, 0.0, -1.0]) - 5 * lr * g / (np.abs(g) + eps)
+    return float(np.abs(p - want).max())
+
+
+def laprop_t2_error():
+    """g1 = 1 then g2 = -2 (b1 .9, b2 .999, eps 0), worked by hand: v2 = .999 *
+    .001 + .001 * 4 = .004999, corrected by 1 - .999^2 = .001999 to 2.50075037...,
+    root 1.58137610...; the normalised gradient -2 / 1.58137610 = -1.26472128
+    joins m1 = .1: m2 = .09 - .126472128 = -.0364721275, over 1 - .81 = .19:
+    p2 = p1 + lr * .191958566.  (Adam, feeding the raw gradient to m, would step
+    by .578947 / 1.581376 = .366104 instead.)"""
+    lr = 0.5
+    p0 = np.array([2.0], np.float32)
+    p1, m1, v1 = oracle.laprop_update(p0, np.array([1.0]), np.zeros(1, np.float32),
+                                      np.zeros(1, np.float32), lr, 1, 0.9, 0.999, 0.0)
+    p2, m2, _ = oracle.laprop_update(p1, np.array([-2.0]), m1, v1, lr, 2, 0.9, 0.999, 0.0)
+    want1 = 2.0 - lr
+    want2 = want1 + lr * 0.1919585659024943
+    return float(max(abs(p1[0] - want1), abs(p2[0] - want2), abs(m2[0] + 0.03647212752147392)))
+
+
+def laprop_scale_invariance_error(seed=5):
+    """With eps = 0 LaProp's steps do not change when every gradient is scaled
+    by the same c > 0 (the gradient enters only through g / sqrt(v))."""
+    r = _rng(seed)
+    gs = [r.standard_normal(16) for _ in range(4)]
+
+    def run(c):
+        p = np.zeros(16, np.float32)
+        m = np.zeros(16, np.float32)
+        v = np.zeros(16, np.float32)
+        for t, g in enumerate(gs, 1):
+            p, m, v = oracle.laprop_update(p, c * g, m, v, 1e-2, t, 0.9, 0.99, 0.0)
+        return p.astype(np.float64)
+
+    a, b = run(1.0), run(37.0)
+    return float(np.abs(a - b).max() / np.abs(a).max())
+
+
+def momentum_error():
+    """Heavy-ball SGD from b = 0: the first step is plain SGD; with a constant
+    gradient b_t = g (1 - mu^t) / (1 - mu), so after four steps p has moved by
+    lr g (1 + 1.9 + 2.71 + 3.439) = 9.049 lr g for mu = .9."""
+    p0 = np.array([1.0, -2.0], np.float32)
+    g = np.array([0.5, -0.25])
+    lr = 0.01
+    p1, b1 = oracle.sgd_momentum_update(p0, g, np.zeros(2, np.float32), lr, 0.9)
+    e1 = np.abs(p1 - oracle.sgd_update(p0, g, lr)).max()
+    p, b = p1, b1
+    for _ in range(3):
+        p, b = oracle.sgd_momentum_update(p, g, b, lr, 0.9)
+    e2 = np.abs(p.astype(np.float64) - (np.array([1.0, -2.0]) - 9.049 * lr * g)).max()
+    e3 = np.abs(b.astype(np.float64) - 3.439 * g).max()
+    return float(max(e1, e2, e3))
+
+
 def gelu_special_error():
     z = np.array([0.0, 20.0, -20.0, 1.0])
     v = oracle.gelu_tanh(z)
@@ -312,6 +396,11 @@ def all_checks():
         ("adam1", lambda: adam_t1_error() < 1e-6),
         ("adam2", lambda: adam_t2_error() < 1e-6),
         ("sgd", lambda: sgd_error() < 1e-7),
+        ("laprop1", lambda: laprop_t1_error() < 1e-6),
+        ("laprop_const", lambda: laprop_constant_gradient_error() < 1e-6),
+        ("laprop2", lambda: laprop_t2_error() < 1e-6),
+        ("laprop_scale", lambda: laprop_scale_invariance_error() < 1e-5),
+        ("momentum", lambda: momentum_error() < 1e-6),
         ("gelu", lambda: gelu_special_error() < 1e-12),
         ("attn_special", lambda: attention_special_error() < 1e-12),
         ("attn_brute", lambda: attention_brute_force_error() < 1e-12),

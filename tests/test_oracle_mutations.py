@@ -41,14 +41,20 @@ MUTATIONS = {
     "attn_heads_swapped_v": ("v = qkv[r, 2 * d + hh * dh: 2 * d + (hh + 1) * dh]",
                              "v = qkv[r, 2 * d + ((hh + 1) % h) * dh: 2 * d + ((hh + 1) % h + 1) * dh]"),
     "adam_no_bias_correction": ("mhat = m2 / (1.0 - beta1 ** step)", "mhat = m2"),
-    "adam_eps_inside": ("(np.sqrt(vhat) + eps)", "np.sqrt(vhat + eps)"),
+    "adam_eps_inside": ("lr * mhat / (np.sqrt(vhat) + eps)", "lr * mhat / np.sqrt(vhat + eps)"),
+    "laprop_raw_gradient_in_momentum": ("(1.0 - beta1) * g / (np.sqrt(vhat) + eps)", "(1.0 - beta1) * g"),
+    "laprop_no_second_moment_correction": ("vhat = v2 / (1.0 - beta2 ** step)\n    m2", "vhat = v2\n    m2"),
+    "laprop_no_momentum_correction": ("lr * m2 / (1.0 - beta1 ** step)", "lr * m2"),
+    "laprop_root_after_eps": ("g / (np.sqrt(vhat) + eps)", "g / np.sqrt(vhat + eps)"),
+    "momentum_dampened": ("b2 = mu * np.asarray(b, np.float64) + g", "b2 = mu * np.asarray(b, np.float64) + (1.0 - mu) * g"),
+    "momentum_old_buffer": ("p2 = np.asarray(p, np.float64) - lr * b2", "p2 = np.asarray(p, np.float64) - lr * (b2 - g)"),
     "sgd_sign": ("return (np.asarray(p, np.float64) - lr * g)", "return (np.asarray(p, np.float64) + lr * g)"),
     "bf16_truncate": ("u + np.uint64(0x7FFF) + lsb", "u"),
 }
 
 NAMES = ["forward", "backward", "loss_and_grad", "train_step", "run_steps", "adam_update",
          "sgd_update", "gelu_tanh", "gelu_tanh_grad", "attention_fwd", "attention_bwd",
-         "bf16_round"]
+         "bf16_round", "laprop_update", "sgd_momentum_update"]
 
 
 def _load_mutant(old, new):
