@@ -314,8 +314,8 @@ def main():
         flat[off:off + r * c] = torch.from_numpy(t.reshape(-1))
     params = flat.cuda()
     grads = torch.zeros_like(params)
-    m = torch.zeros_like(params) if w.optimizer == "adam" else None
-    v = torch.zeros_like(params) if w.optimizer == "adam" else None
+    m = torch.zeros_like(params) if w.optimizer in ("adam", "laprop", "sgd_momentum") else None
+    v = torch.zeros_like(params) if w.optimizer in ("adam", "laprop") else None
     x = W.make_x(w)
     y = W.make_labels(w)
     xt = torch.from_numpy(x)

@@ -62,7 +62,17 @@ typedef enum {
 
 typedef enum { MG_LOSS_CE_DENSE = 0, MG_LOSS_CE_INDEX = 1, MG_LOSS_MSE = 2 } mg_loss_kind;
 typedef enum { MG_PREC_STRICT_F32 = 0, MG_PREC_BF16 = 1 } mg_precision;
-typedef enum { MG_OPT_SGD = 0, MG_OPT_ADAM = 1 } mg_optimizer;
+/* SGD: p -= lr g.  ADAM: bias-corrected moments, eps after the root.  LAPROP
+ * (named beside Adam in the paper's checkpoint notes; the update is the
+ * published LaProp algorithm): v = b2 v + (1-b2) g^2, m = b1 m + (1-b1) g /
+ * (sqrt(v / (1 - b2^t)) + eps), p -= lr m / (1 - b1^t).  SGD_MOMENTUM:
+ * heavy ball, b = beta1 b + g, p -= lr b (beta1 is the momentum). */
+typedef enum {
+  MG_OPT_SGD = 0,
+  MG_OPT_ADAM = 1,
+  MG_OPT_LAPROP = 2,
+  MG_OPT_SGD_MOMENTUM = 3
+} mg_optimizer;
 
 typedef struct {
   int op;        /* mg_op */
@@ -117,11 +127,13 @@ mg_status mg_forward(mg_plan* plan, const float* params, const void* x, float* o
 /* One full training step: forward, loss, backward, optimizer update.
  *  params  fp32 [P]  updated in place (fp32 master weights)
  *  grads   fp32 [P]  overwritten with dLoss/dparams of this step (before the update)
- *  adam_m, adam_v fp32 [P]  Adam moments, updated in place; may be NULL under SGD
+ *  adam_m, adam_v fp32 [P]  optimizer state, updated in place: Adam and LaProp
+ *          use both (first and second moment); SGD_MOMENTUM keeps its velocity
+ *          in adam_m (adam_v may be NULL); plain SGD needs neither
  *  x       [batch, d_in], fp32 (strict) or bf16 (bf16)
  *  labels  CE_DENSE: fp32 [batch, C]; CE_INDEX: int32 [batch], values in [0, C);
  *          MSE: target [batch, d_out] in the activation dtype (fp32 / bf16)
- *  lr      learning rate; step: Adam's t, 1-based (ignored by SGD)
+ *  lr      learning rate; step: Adam's / LaProp's t, 1-based (ignored by SGD)
  * The loss of the step is kept on the device (mg_loss, mg_loss_device_ptr).
  * grads must not alias params.  The bf16 weight copy used by the bf16 path is
  * refreshed from params automatically when step == 1 or params differs from the

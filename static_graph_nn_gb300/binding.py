@@ -23,7 +23,7 @@ OPS = {"linear": 0, "relu": 1, "gelu_tanh": 2, "rmsnorm": 3, "residual_begin": 4
        "residual_end": 5, "causal_attention": 6}
 LOSSES = {"ce_dense": 0, "ce_index": 1, "mse": 2}
 PRECISIONS = {"strict": 0, "bf16": 1}
-OPTIMIZERS = {"sgd": 0, "adam": 1}
+OPTIMIZERS = {"sgd": 0, "adam": 1, "laprop": 2, "sgd_momentum": 3}
 
 
 class mg_layer(ctypes.Structure):

@@ -95,6 +95,11 @@ struct Chunk {  // a run of one tensor's elements in the flat buffers
 cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
                         float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
                         float beta1, float beta2, float eps, cudaStream_t s);
+cudaError_t laprop_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
+                          float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
+                          float beta1, float beta2, float eps, cudaStream_t s);
+cudaError_t momentum_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* b,
+                            void* shadow, float lr, float mu, cudaStream_t s);
 cudaError_t sgd_update(const Chunk* chunks, int n_chunks, float* p, const float* g, void* shadow,
                        float lr, cudaStream_t s);
 cudaError_t cast_shadow(const Chunk* chunks, int n_chunks, const float* p, void* shadow,

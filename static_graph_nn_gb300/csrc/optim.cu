@@ -7,6 +7,11 @@
 //
 // Adam (t = step, 1-based): m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2,
 // p -= (lr / (1 - b1^t)) m / (sqrt(v) / sqrt(1 - b2^t) + eps).
+// LaProp (the published algorithm of Ziyin, Wang & Ueda, 2020; the paper's
+// checkpoint notes name it beside Adam): v = b2 v + (1-b2) g^2,
+// m = b1 m + (1-b1) g / (sqrt(v) / sqrt(1 - b2^t) + eps),
+// p -= (lr / (1 - b1^t)) m.
+// SGD with heavy-ball momentum mu: b = mu b + g, p -= lr b.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -60,6 +65,82 @@ __global__ void __launch_bounds__(256) adam_kernel(const Chunk* chunks, float* p
   }
 }
 
+__device__ __forceinline__ void laprop_one(float& p, float g, float& m, float& v, float lr_bc1,
+                                           float inv_sqrt_bc2, float b1, float b2, float eps) {
+  v = b2 * v + (1.0f - b2) * g * g;
+  m = b1 * m + (1.0f - b1) * g / (sqrtf(v) * inv_sqrt_bc2 + eps);
+  p -= lr_bc1 * m;
+}
+
+__device__ __forceinline__ void shadow4(bf16* shadow, long long base, int i, const float4& pp) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(pp.z, pp.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(shadow + base)[i] = packed;
+}
+
+__global__ void __launch_bounds__(256) laprop_kernel(const Chunk* chunks, float* p, const float* g,
+                                                     float* m, float* v, bf16* shadow, float lr_bc1,
+                                                     float inv_sqrt_bc2, float b1, float b2,
+                                                     float eps) {
+  const Chunk c = chunks[blockIdx.x];
+  const long long base = c.start;
+  const int n4 = c.len >> 2;
+  float4* p4 = reinterpret_cast<float4*>(p + base);
+  const float4* g4 = reinterpret_cast<const float4*>(g + base);
+  float4* m4 = reinterpret_cast<float4*>(m + base);
+  float4* v4 = reinterpret_cast<float4*>(v + base);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 pp = p4[i], gg = g4[i], mm = m4[i], vv = v4[i];
+    laprop_one(pp.x, gg.x, mm.x, vv.x, lr_bc1, inv_sqrt_bc2, b1, b2, eps);
+    laprop_one(pp.y, gg.y, mm.y, vv.y, lr_bc1, inv_sqrt_bc2, b1, b2, eps);
+    laprop_one(pp.z, gg.z, mm.z, vv.z, lr_bc1, inv_sqrt_bc2, b1, b2, eps);
+    laprop_one(pp.w, gg.w, mm.w, vv.w, lr_bc1, inv_sqrt_bc2, b1, b2, eps);
+    p4[i] = pp;
+    m4[i] = mm;
+    v4[i] = vv;
+    if (shadow && c.shadow) shadow4(shadow, base, i, pp);
+  }
+  for (int i = (n4 << 2) + threadIdx.x; i < c.len; i += blockDim.x) {
+    long long k = base + i;
+    float pp = p[k], mm = m[k], vv = v[k];
+    laprop_one(pp, g[k], mm, vv, lr_bc1, inv_sqrt_bc2, b1, b2, eps);
+    p[k] = pp;
+    m[k] = mm;
+    v[k] = vv;
+    if (shadow && c.shadow) shadow[k] = __float2bfloat16_rn(pp);
+  }
+}
+
+__global__ void __launch_bounds__(256) momentum_kernel(const Chunk* chunks, float* p,
+                                                       const float* g, float* b, bf16* shadow,
+                                                       float lr, float mu) {
+  const Chunk c = chunks[blockIdx.x];
+  const long long base = c.start;
+  const int n4 = c.len >> 2;
+  float4* p4 = reinterpret_cast<float4*>(p + base);
+  const float4* g4 = reinterpret_cast<const float4*>(g + base);
+  float4* b4 = reinterpret_cast<float4*>(b + base);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    float4 pp = p4[i], gg = g4[i], bb = b4[i];
+    bb.x = mu * bb.x + gg.x; bb.y = mu * bb.y + gg.y; bb.z = mu * bb.z + gg.z; bb.w = mu * bb.w + gg.w;
+    pp.x -= lr * bb.x; pp.y -= lr * bb.y; pp.z -= lr * bb.z; pp.w -= lr * bb.w;
+    p4[i] = pp;
+    b4[i] = bb;
+    if (shadow && c.shadow) shadow4(shadow, base, i, pp);
+  }
+  for (int i = (n4 << 2) + threadIdx.x; i < c.len; i += blockDim.x) {
+    long long k = base + i;
+    const float bb = mu * b[k] + g[k];
+    const float pp = p[k] - lr * bb;
+    b[k] = bb;
+    p[k] = pp;
+    if (shadow && c.shadow) shadow[k] = __float2bfloat16_rn(pp);
+  }
+}
+
 __global__ void __launch_bounds__(256) sgd_kernel(const Chunk* chunks, float* p, const float* g,
                                                   bf16* shadow, float lr) {
   const Chunk c = chunks[blockIdx.x];
@@ -102,6 +183,22 @@ cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float
   if (n_chunks <= 0) return cudaSuccess;
   adam_kernel<<<n_chunks, 256, 0, s>>>(chunks, p, g, m, v, (bf16*)shadow, lr_over_bc1,
                                        inv_sqrt_bc2, beta1, beta2, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t laprop_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
+                          float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
+                          float beta1, float beta2, float eps, cudaStream_t s) {
+  if (n_chunks <= 0) return cudaSuccess;
+  laprop_kernel<<<n_chunks, 256, 0, s>>>(chunks, p, g, m, v, (bf16*)shadow, lr_over_bc1,
+                                         inv_sqrt_bc2, beta1, beta2, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t momentum_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* b,
+                            void* shadow, float lr, float mu, cudaStream_t s) {
+  if (n_chunks <= 0) return cudaSuccess;
+  momentum_kernel<<<n_chunks, 256, 0, s>>>(chunks, p, g, b, (bf16*)shadow, lr, mu);
   return cudaGetLastError();
 }
 

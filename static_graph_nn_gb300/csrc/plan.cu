@@ -344,14 +344,22 @@ void node_update(Exec& e, int ni) {
     if (r != cudaSuccess) e.err = r;
   }
   char nm[96];
-  if (p->optimizer == MG_OPT_ADAM) {
+  if (p->optimizer == MG_OPT_ADAM || p->optimizer == MG_OPT_LAPROP) {
     double bc1 = 1.0 - std::pow((double)p->beta1, (double)e.step);
     double bc2 = 1.0 - std::pow((double)p->beta2, (double)e.step);
     float lr_bc1 = (float)(e.lr / bc1), inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
-    snprintf(nm, sizeof nm, "adam[l%d] %.0f params", n.layer, np);
+    const bool lap = p->optimizer == MG_OPT_LAPROP;
+    snprintf(nm, sizeof nm, "%s[l%d] %.0f params", lap ? "laprop" : "adam", n.layer, np);
     site_on(e, p->aux, nm, 0, np * (28.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
-      return adam_update(chunks, c1 - c0, e.params, e.grads, e.m, e.v, shadow, lr_bc1,
-                         inv_sqrt_bc2, p->beta1, p->beta2, p->adam_eps, p->aux);
+      return (lap ? laprop_update : adam_update)(chunks, c1 - c0, e.params, e.grads, e.m, e.v,
+                                                 shadow, lr_bc1, inv_sqrt_bc2, p->beta1,
+                                                 p->beta2, p->adam_eps, p->aux);
+    });
+  } else if (p->optimizer == MG_OPT_SGD_MOMENTUM) {
+    snprintf(nm, sizeof nm, "momentum[l%d] %.0f params", n.layer, np);
+    site_on(e, p->aux, nm, 0, np * (20.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
+      return momentum_update(chunks, c1 - c0, e.params, e.grads, e.m, shadow, e.lr, p->beta1,
+                             p->aux);
     });
   } else {
     snprintf(nm, sizeof nm, "sgd[l%d] %.0f params", n.layer, np);
@@ -485,11 +493,13 @@ mg_status compile(mg_plan* p, const mg_graph_desc* d) {
   if (d->loss < 0 || d->loss > 2) return fail(p, MG_ERR_INVALID_ARG, "bad loss kind %d", d->loss);
   if (d->precision < 0 || d->precision > 1)
     return fail(p, MG_ERR_INVALID_ARG, "bad precision %d", d->precision);
-  if (d->optimizer < 0 || d->optimizer > 1)
+  if (d->optimizer < MG_OPT_SGD || d->optimizer > MG_OPT_SGD_MOMENTUM)
     return fail(p, MG_ERR_INVALID_ARG, "bad optimizer %d", d->optimizer);
-  if (d->optimizer == MG_OPT_ADAM &&
+  if ((d->optimizer == MG_OPT_ADAM || d->optimizer == MG_OPT_LAPROP) &&
       !(d->beta1 >= 0 && d->beta1 < 1 && d->beta2 >= 0 && d->beta2 < 1 && d->adam_eps > 0))
-    return fail(p, MG_ERR_INVALID_ARG, "Adam needs 0 <= beta < 1 and eps > 0");
+    return fail(p, MG_ERR_INVALID_ARG, "Adam and LaProp need 0 <= beta < 1 and eps > 0");
+  if (d->optimizer == MG_OPT_SGD_MOMENTUM && !(d->beta1 >= 0 && d->beta1 < 1))
+    return fail(p, MG_ERR_INVALID_ARG, "momentum (beta1) must be in [0, 1)");
   p->batch = d->batch;
   p->loss = d->loss;
   p->precision = d->precision;
@@ -724,7 +734,11 @@ void build_dump(mg_plan* p) {
   char b[256];
   snprintf(b, sizeof b, "plan: batch %d, %s, %s, loss %d, %zu params, workspace %zu bytes\n",
            p->batch, p->dt == DT_BF16 ? "bf16" : "strict-f32",
-           p->optimizer == MG_OPT_ADAM ? "adam" : "sgd", p->loss, p->n_params, p->ws_bytes);
+           p->optimizer == MG_OPT_ADAM     ? "adam"
+           : p->optimizer == MG_OPT_LAPROP ? "laprop"
+           : p->optimizer == MG_OPT_SGD    ? "sgd"
+                                           : "sgd_momentum",
+           p->loss, p->n_params, p->ws_bytes);
   s += b;
   for (size_t i = 0; i < p->p_off.size(); ++i) {
     snprintf(b, sizeof b, "  param %zu: offset %zu [%d x %d]\n", i, p->p_off[i], p->p_rows[i],
@@ -886,9 +900,12 @@ mg_status mg_train_step(mg_plan* p, float* params, float* grads, float* adam_m, 
   if (!p) return fail(nullptr, MG_ERR_INVALID_ARG, "plan is NULL");
   if (!params || !grads || !x || !labels)
     return fail(p, MG_ERR_INVALID_ARG, "params, grads, x and labels must be non-NULL");
-  if (p->optimizer == MG_OPT_ADAM && (!adam_m || !adam_v))
-    return fail(p, MG_ERR_INVALID_ARG, "Adam needs adam_m and adam_v");
-  if (p->optimizer == MG_OPT_ADAM && step < 1) return fail(p, MG_ERR_INVALID_ARG, "step must be >= 1");
+  const bool two_moments = p->optimizer == MG_OPT_ADAM || p->optimizer == MG_OPT_LAPROP;
+  if (two_moments && (!adam_m || !adam_v))
+    return fail(p, MG_ERR_INVALID_ARG, "Adam and LaProp need adam_m and adam_v");
+  if (p->optimizer == MG_OPT_SGD_MOMENTUM && !adam_m)
+    return fail(p, MG_ERR_INVALID_ARG, "SGD with momentum keeps its velocity in adam_m");
+  if (two_moments && step < 1) return fail(p, MG_ERR_INVALID_ARG, "step must be >= 1");
   if (!aligned16(params) || !aligned16(grads) || !aligned16(x) || !aligned16(labels) ||
       (adam_m && !aligned16(adam_m)) || (adam_v && !aligned16(adam_v)))
     return fail(p, MG_ERR_ALIGN, "buffers must be 16-byte aligned");

@@ -110,7 +110,7 @@ class Workload:
     layers: list
     loss: str                  # "ce_dense" | "ce_index" | "mse"
     precisions: tuple          # subset of ("strict", "bf16")
-    optimizer: str             # "sgd" | "adam"
+    optimizer: str             # "sgd" | "adam" | "laprop" | "sgd_momentum"
     lr: float
     steps: int
     init: str                  # "he_normal" | "xavier_uniform" | "normal002"

@@ -61,14 +61,17 @@ class Device:
         n = plan.param_count
         self.params = torch.zeros(n, dtype=torch.float32, device="cuda")
         self.grads = torch.zeros_like(self.params)
-        self.m = torch.zeros_like(self.params) if w.optimizer == "adam" else None
-        self.v = torch.zeros_like(self.params) if w.optimizer == "adam" else None
+        has_m, has_v = oracle.MOMENTS[w.optimizer]
+        self.m = torch.zeros_like(self.params) if has_m else None
+        self.v = torch.zeros_like(self.params) if has_v else None
 
     def load(self, params, m=None, v=None):
         self.params.copy_(pack(self.plan, params))
+        zeros = [np.zeros_like(a) for a in params]
         if self.m is not None:
-            self.m.copy_(pack(self.plan, m if m is not None else [np.zeros_like(a) for a in params]))
-            self.v.copy_(pack(self.plan, v if v is not None else [np.zeros_like(a) for a in params]))
+            self.m.copy_(pack(self.plan, m if m is not None else zeros))
+        if self.v is not None:
+            self.v.copy_(pack(self.plan, v if v is not None else zeros))
         self.plan.refresh_params(self.params)
 
     def read(self):
@@ -76,6 +79,7 @@ class Device:
                "params": unpack(self.plan, self.params, self.shapes)}
         if self.m is not None:
             out["adam_m"] = unpack(self.plan, self.m, self.shapes)
+        if self.v is not None:
             out["adam_v"] = unpack(self.plan, self.v, self.shapes)
         return out
 
@@ -108,22 +112,29 @@ def cosine(a, b):
     return float(a @ b / (na * nb))
 
 
-def update_band(w, p, g, m, v, t, dg):
-    """How far the oracle's own update of p moves when its gradient moves
-    anywhere within +-dg (sampled at 9 points): the part of an updated parameter
-    that the gradient gate leaves undetermined.  Near g = 0 Adam's normalised
-    step can take either sign."""
-    base = _oracle_update(w, p, g, m, v, t)
+def update_band(w, p, g, m, v, t, dg, part=0):
+    """How far the oracle's own update of p (part 0), or of its first / second
+    moment (parts 1, 2), moves when its gradient moves anywhere within +-dg
+    (sampled at 9 points): the part of an updated state that the gradient gate
+    leaves undetermined.  Near g = 0 a normalised step can take either sign."""
+    base = _oracle_update(w, p, g, m, v, t)[part]
     band = np.zeros_like(base)
     for f in np.linspace(-1.0, 1.0, 9):
-        band = np.maximum(band, np.abs(_oracle_update(w, p, g + f * dg, m, v, t) - base))
+        band = np.maximum(band, np.abs(_oracle_update(w, p, g + f * dg, m, v, t)[part] - base))
     return band
 
 
 def _oracle_update(w, p, g, m, v, t):
+    """The oracle's (p, m, v) after one update, float64 (None for state the
+    optimizer does not keep)."""
+    f = lambda a: None if a is None else np.asarray(a, np.float64)
     if w.optimizer == "sgd":
-        return oracle.sgd_update(p, g, w.lr).astype(np.float64)
-    return oracle.adam_update(p, g, m, v, w.lr, t, w.beta1, w.beta2, w.adam_eps)[0].astype(np.float64)
+        return f(oracle.sgd_update(p, g, w.lr)), None, None
+    if w.optimizer == "sgd_momentum":
+        a, b = oracle.sgd_momentum_update(p, g, m, w.lr, w.beta1)
+        return f(a), f(b), None
+    upd = oracle.adam_update if w.optimizer == "adam" else oracle.laprop_update
+    return tuple(f(a) for a in upd(p, g, m, v, w.lr, t, w.beta1, w.beta2, w.adam_eps))
 
 
 def adam_step_bound(w):
@@ -131,6 +142,21 @@ def adam_step_bound(w):
     most (1-b1)/sqrt(1-b2) when (1-b1) > sqrt(1-b2), else 1 (Kingma & Ba, 2015,
     section 2.1), so two runs from the same state differ by at most twice that."""
     return 2.0 * w.lr * max(1.0, (1 - w.beta1) / math.sqrt(1 - w.beta2))
+
+
+def step_bound(w, g, m_prev):
+    """Twice the largest |update| one step of the workload's optimizer can make
+    (two runs from the same state differ by at most that).  LaProp: every
+    normalised gradient g / sqrt(v_hat) is at most 1 / sqrt(1 - b2) in size
+    (v >= (1 - b2) g^2 and the correction divides by at most 1), and the step
+    is a weighted average of them.  Momentum: lr (mu |b| + |g|)."""
+    if w.optimizer == "adam":
+        return adam_step_bound(w)
+    if w.optimizer == "laprop":
+        return 2.0 * w.lr / math.sqrt(1 - w.beta2)
+    if w.optimizer == "sgd_momentum":
+        return 2.0 * w.lr * (w.beta1 * float(np.abs(m_prev).max()) + float(np.abs(g).max()))
+    return 2 * w.lr * float(np.abs(g).max())
 
 
 def compare(w, precision, steps):
@@ -175,19 +201,20 @@ def compare(w, precision, steps):
                 e = float(max(excess.max(), 0.0) / max(np.abs(pb).max(), 1e-30))
                 worst["params"] = max(worst["params"], e)
                 assert e <= STRICT_TOL, f"step {t}: param {n} max rel err {e:.3g} beyond band"
-                if w.optimizer == "adam":
-                    for key, bandk in (("adam_m", (1 - w.beta1) * dg),
-                                       ("adam_v", (1 - w.beta2) * (2 * np.abs(b) * dg + dg * dg))):
-                        ma, mb = g[key][i], o[key][i].astype(np.float64)
-                        excess = np.abs(ma - mb) - bandk - np.abs(mb) * 2.0 ** -22
-                        e = float(max(excess.max(), 0.0) / max(np.abs(mb).max(), 1e-30))
-                        assert e <= STRICT_TOL, f"step {t}: {key} {n} max rel err {e:.3g}"
+                for part, key in ((1, "adam_m"), (2, "adam_v")):
+                    if key not in g:
+                        continue
+                    bandk = update_band(w, prev_p[i], b, prev_m[i], prev_v[i], t, dg, part)
+                    ma, mb = g[key][i], o[key][i].astype(np.float64)
+                    excess = np.abs(ma - mb) - bandk - np.abs(mb) * 2.0 ** -22
+                    e = float(max(excess.max(), 0.0) / max(np.abs(mb).max(), 1e-30))
+                    assert e <= STRICT_TOL, f"step {t}: {key} {n} max rel err {e:.3g}"
             else:
                 c = cosine(a, b)
                 worst["grads"] = min(worst["grads"], c)
                 assert c >= BF16_COSINE, f"step {t}: grad {n} cosine {c:.6f}"
                 d = float(np.abs(g["params"][i] - o["params"][i]).max())
-                bound = adam_step_bound(w) if w.optimizer == "adam" else 2 * w.lr * np.abs(b).max()
+                bound = step_bound(w, b, prev_m[i])
                 worst["params"] = max(worst["params"], d / bound)
                 assert d <= bound + 1e-6, f"step {t}: param {n} moved {d:.3g} from the oracle's"
         state = (o["params"], o["adam_m"] or None, o["adam_v"] or None)

@@ -58,7 +58,17 @@ CASES = {
     "ragged_strict": (ragged, "strict", 3),
     "ragged_bf16": (ragged, "bf16", 3),
     "ragged_sgd_strict": (lambda: _sgd(ragged()), "strict", 2),
+    "ragged_laprop_strict": (lambda: _opt(ragged(), "laprop", 1e-3), "strict", 3),
+    "ragged_laprop_bf16": (lambda: _opt(ragged(), "laprop", 1e-3), "bf16", 3),
+    "ragged_momentum_strict": (lambda: _opt(ragged(), "sgd_momentum", 0.05), "strict", 3),
+    "ragged_momentum_bf16": (lambda: _opt(ragged(), "sgd_momentum", 0.05), "bf16", 3),
 }
+
+
+def _opt(w, name, lr):
+    w.optimizer = name
+    w.lr = lr
+    return w
 
 
 def _sgd(w):
