@@ -152,6 +152,35 @@ const float* mg_loss_device_ptr(const mg_plan* plan);
  * e.g. a checkpoint restore).  A no-op in strict mode. */
 mg_status mg_refresh_params(mg_plan* plan, const float* params, mg_stream_t stream);
 
+/* ---- checkpoints --------------------------------------------------------
+ * The paper's checkpoint notes: a checkpoint stores the logical tensors (no
+ * device padding) and a restore is checked in full before it changes
+ * anything.  Host-memory image, little-endian:
+ *   64-byte header: magic "MGCKPT\0\1", u32 version (1), u32 tensor count,
+ *     u32 flags (bit 0: first moment stored, bit 1: second moment stored),
+ *     u32 precision of the saving plan, u64 values per section, u64 checksum
+ *     of the sections, 24 reserved bytes;
+ *   per tensor (mg_param_info order): u32 rows, u32 cols;
+ *   sections, fp32: params, then the first moment, then the second moment,
+ *     each the tensors' values back to back.
+ * mg_checkpoint_bytes: the image size with the given sections.
+ * mg_checkpoint_save: params (and m, v when non-NULL; v needs m) from the
+ *   device into host_buf (cap bytes); *written gets the size; synchronises
+ *   stream.  MG_ERR_INVALID_ARG when cap is too small.
+ * mg_checkpoint_load: checks magic, version, tensor count and every shape
+ *   against this plan, the size, the requested sections' presence and the
+ *   checksum -- any failure returns an error with no device memory changed --
+ *   then copies params (and m, v when non-NULL; moments stored but not asked
+ *   for are skipped, e.g. when a forward-only or SGD plan takes a trained
+ *   model) and refreshes the bf16 weight copy; synchronises stream.  The
+ *   plan may differ from the saving one in everything but the tensors'
+ *   shapes (precision, optimizer, batch). */
+size_t mg_checkpoint_bytes(const mg_plan* plan, int with_m, int with_v);
+mg_status mg_checkpoint_save(mg_plan* plan, const float* params, const float* m, const float* v,
+                             void* host_buf, size_t cap, size_t* written, mg_stream_t stream);
+mg_status mg_checkpoint_load(mg_plan* plan, const void* host_buf, size_t len, float* params,
+                             float* m, float* v, mg_stream_t stream);
+
 /* Human-readable schedule: one line per kernel with its shapes and the
  * workspace offsets (the analogue of the pages' plan dump).  Writes at most
  * cap bytes including the terminating NUL; returns the full length. */

@@ -63,6 +63,10 @@ _SIGS = {
     "mg_profile_entries": (ctypes.c_int, [_P]),
     "mg_softmax_ce_noalloc": (ctypes.c_int, [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, _P, _P, _P, _P]),
+    "mg_checkpoint_bytes": (ctypes.c_size_t, [_P, ctypes.c_int, ctypes.c_int]),
+    "mg_checkpoint_save": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.POINTER(ctypes.c_size_t), _P]),
+    "mg_checkpoint_load": (ctypes.c_int, [_P, ctypes.c_void_p, ctypes.c_size_t, _P, _P, _P, _P]),
     "mg_profile_entry": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_char_p, ctypes.c_size_t,
                                         ctypes.POINTER(ctypes.c_int),
                                         ctypes.POINTER(ctypes.c_double),
@@ -202,6 +206,22 @@ class Plan:
 
     def refresh_params(self, params, stream=None):
         self._check(self.lib.mg_refresh_params(self.h, _ptr(params), _stream(stream)))
+
+    def checkpoint_save(self, params, m=None, v=None, stream=None) -> bytes:
+        """The checkpoint image of params (and moments when given) as bytes."""
+        n = self.lib.mg_checkpoint_bytes(self.h, int(m is not None), int(v is not None))
+        buf = ctypes.create_string_buffer(n)
+        written = ctypes.c_size_t()
+        self._check(self.lib.mg_checkpoint_save(self.h, _ptr(params), _ptr(m), _ptr(v), buf, n,
+                                                ctypes.byref(written), _stream(stream)))
+        return buf.raw[:written.value]
+
+    def checkpoint_load(self, image: bytes, params, m=None, v=None, stream=None):
+        """Restore params (and moments when given) from a checkpoint image; the
+        image is checked in full first and nothing changes if it fails."""
+        buf = ctypes.create_string_buffer(bytes(image), len(image))
+        self._check(self.lib.mg_checkpoint_load(self.h, buf, len(image), _ptr(params), _ptr(m),
+                                                _ptr(v), _stream(stream)))
 
     def dump(self) -> str:
         n = self.lib.mg_plan_dump(self.h, None, 0)

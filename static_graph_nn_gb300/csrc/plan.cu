@@ -964,6 +964,155 @@ mg_status mg_refresh_params(mg_plan* p, const float* params, mg_stream_t stream)
   return MG_OK;
 }
 
+// ---- checkpoints -------------------------------------------------------------
+// The paper's checkpoint notes: logical tensors without device padding, and a
+// restore that is checked before anything is changed.  Layout (little-endian):
+// a 64-byte header (magic, version, tensor count, section flags, precision,
+// floats per section, checksum), the tensors' (rows, cols), then the sections
+// params, first moment, second moment, each the tensors' values back to back.
+namespace {
+
+constexpr char kCkptMagic[8] = {'M', 'G', 'C', 'K', 'P', 'T', 0, 1};
+constexpr uint32_t kCkptVersion = 1;
+constexpr size_t kCkptHeader = 64;
+
+struct CkptHeader {
+  char magic[8];
+  uint32_t version, n_tensors, flags, precision;
+  uint64_t floats, checksum;
+  uint8_t reserved[24];
+};
+static_assert(sizeof(CkptHeader) == kCkptHeader, "checkpoint header is 64 bytes");
+
+size_t logical_floats(const mg_plan* p) {
+  size_t n = 0;
+  for (size_t t = 0; t < p->p_off.size(); ++t) n += (size_t)p->p_rows[t] * p->p_cols[t];
+  return n;
+}
+
+size_t ckpt_bytes(const mg_plan* p, int sections) {
+  return kCkptHeader + 8 * p->p_off.size() + 4 * logical_floats(p) * sections;
+}
+
+// 64-bit multiply-xorshift hash of the data sections, eight bytes at a time.
+uint64_t ckpt_hash(const uint8_t* d, size_t n) {
+  uint64_t h = 0x9E3779B97F4A7C15ull ^ n;
+  size_t i = 0;
+  for (; i + 8 <= n; i += 8) {
+    uint64_t w;
+    memcpy(&w, d + i, 8);
+    h = (h ^ w) * 0xBF58476D1CE4E5B9ull;
+    h ^= h >> 31;
+  }
+  for (; i < n; ++i) h = (h ^ d[i]) * 0x100000001B3ull;
+  return h ^ (h >> 29);
+}
+
+}  // namespace
+
+size_t mg_checkpoint_bytes(const mg_plan* p, int with_m, int with_v) {
+  if (!p) return 0;
+  return ckpt_bytes(p, 1 + (with_m ? 1 : 0) + (with_v ? 1 : 0));
+}
+
+mg_status mg_checkpoint_save(mg_plan* p, const float* params, const float* m, const float* v,
+                             void* host_buf, size_t cap, size_t* written, mg_stream_t stream) {
+  if (!p || !params || !host_buf) return fail(p, MG_ERR_INVALID_ARG, "plan, params and buffer must be non-NULL");
+  if (!m && v) return fail(p, MG_ERR_INVALID_ARG, "a second moment without a first one");
+  const int sections = 1 + (m ? 1 : 0) + (v ? 1 : 0);
+  const size_t need = ckpt_bytes(p, sections);
+  if (written) *written = 0;
+  if (cap < need) return fail(p, MG_ERR_INVALID_ARG, "checkpoint needs %zu bytes, buffer has %zu", need, cap);
+  cudaSetDevice(p->device);
+  uint8_t* out = static_cast<uint8_t*>(host_buf);
+  const size_t nt = p->p_off.size(), lf = logical_floats(p);
+  uint8_t* data = out + kCkptHeader + 8 * nt;
+  const float* src[3] = {params, m, v};
+  for (int sct = 0; sct < sections; ++sct) {
+    float* dst = reinterpret_cast<float*>(data + 4 * lf * sct);
+    for (size_t t = 0; t < nt; ++t) {
+      const size_t len = (size_t)p->p_rows[t] * p->p_cols[t];
+      cudaError_t e = cudaMemcpyAsync(dst, src[sct] + p->p_off[t], len * 4, cudaMemcpyDeviceToHost,
+                                      (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(p, e, "checkpoint save copy");
+      dst += len;
+    }
+  }
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "checkpoint save");
+  CkptHeader h;
+  memset(&h, 0, sizeof h);
+  memcpy(h.magic, kCkptMagic, 8);
+  h.version = kCkptVersion;
+  h.n_tensors = (uint32_t)nt;
+  h.flags = (m ? 1u : 0u) | (v ? 2u : 0u);
+  h.precision = (uint32_t)p->precision;
+  h.floats = lf;
+  h.checksum = ckpt_hash(data, 4 * lf * sections);
+  memcpy(out, &h, sizeof h);
+  for (size_t t = 0; t < nt; ++t) {
+    const uint32_t rc[2] = {(uint32_t)p->p_rows[t], (uint32_t)p->p_cols[t]};
+    memcpy(out + kCkptHeader + 8 * t, rc, 8);
+  }
+  if (written) *written = need;
+  return MG_OK;
+}
+
+mg_status mg_checkpoint_load(mg_plan* p, const void* host_buf, size_t len, float* params,
+                             float* m, float* v, mg_stream_t stream) {
+  if (!p || !host_buf || !params) return fail(p, MG_ERR_INVALID_ARG, "plan, buffer and params must be non-NULL");
+  // ---- preflight: every check before the first write
+  if (!aligned16(params) || (m && !aligned16(m)) || (v && !aligned16(v)))
+    return fail(p, MG_ERR_ALIGN, "params and moments must be 16-byte aligned");
+  const uint8_t* in = static_cast<const uint8_t*>(host_buf);
+  if (len < kCkptHeader) return fail(p, MG_ERR_INVALID_ARG, "checkpoint: %zu bytes is shorter than the header", len);
+  CkptHeader h;
+  memcpy(&h, in, sizeof h);
+  if (memcmp(h.magic, kCkptMagic, 8) != 0) return fail(p, MG_ERR_INVALID_ARG, "checkpoint: bad magic");
+  if (h.version != kCkptVersion) return fail(p, MG_ERR_UNSUPPORTED, "checkpoint: version %u", h.version);
+  const size_t nt = p->p_off.size(), lf = logical_floats(p);
+  if (h.n_tensors != nt)
+    return fail(p, MG_ERR_SHAPE, "checkpoint holds %u tensors, the plan has %zu", h.n_tensors, nt);
+  if (h.floats != lf) return fail(p, MG_ERR_SHAPE, "checkpoint holds %llu values per section, the plan %zu",
+                                  (unsigned long long)h.floats, lf);
+  if (h.flags & ~3u || ((h.flags & 2u) && !(h.flags & 1u)))
+    return fail(p, MG_ERR_INVALID_ARG, "checkpoint: bad section flags %u", h.flags);
+  const int sections = 1 + ((h.flags & 1u) ? 1 : 0) + ((h.flags & 2u) ? 1 : 0);
+  if (len != ckpt_bytes(p, sections))
+    return fail(p, MG_ERR_SHAPE, "checkpoint is %zu bytes, its header describes %zu", len, ckpt_bytes(p, sections));
+  for (size_t t = 0; t < nt; ++t) {
+    uint32_t rc[2];
+    memcpy(rc, in + kCkptHeader + 8 * t, 8);
+    if ((int)rc[0] != p->p_rows[t] || (int)rc[1] != p->p_cols[t])
+      return fail(p, MG_ERR_SHAPE, "checkpoint tensor %zu is %ux%u, the plan's is %dx%d", t, rc[0], rc[1],
+                  p->p_rows[t], p->p_cols[t]);
+  }
+  if (m && !(h.flags & 1u)) return fail(p, MG_ERR_INVALID_ARG, "checkpoint has no first moment");
+  if (v && !(h.flags & 2u)) return fail(p, MG_ERR_INVALID_ARG, "checkpoint has no second moment");
+  const uint8_t* data = in + kCkptHeader + 8 * nt;
+  if (ckpt_hash(data, 4 * lf * sections) != h.checksum)
+    return fail(p, MG_ERR_INVALID_ARG, "checkpoint: checksum mismatch (corrupted data)");
+  // ---- restore
+  cudaSetDevice(p->device);
+  float* dst[3] = {params, m, v};
+  for (int sct = 0; sct < 3; ++sct) {
+    if (!dst[sct]) continue;
+    const float* src = reinterpret_cast<const float*>(data + 4 * lf * sct);
+    for (size_t t = 0; t < nt; ++t) {
+      const size_t n = (size_t)p->p_rows[t] * p->p_cols[t];
+      cudaError_t e = cudaMemcpyAsync(dst[sct] + p->p_off[t], src, n * 4, cudaMemcpyHostToDevice,
+                                      (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(p, e, "checkpoint restore copy");
+      src += n;
+    }
+  }
+  mg_status st = mg_refresh_params(p, params, stream);
+  if (st != MG_OK) return st;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "checkpoint restore");
+  return MG_OK;
+}
+
 size_t mg_plan_dump(const mg_plan* p, char* buf, size_t cap) {
   if (!p) return 0;
   if (buf && cap) {
