@@ -13,6 +13,7 @@
 //   SGD / Adam                                    -> one multi-tensor kernel
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -106,6 +107,8 @@ struct mg_plan {
   const float* last_params = nullptr;
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
   bool use_pair = true;      // SM-pair GEMMs for large shapes (MG_GEMM=tc1 turns them off)
+  bool alias = true;         // gradient buffers share storage by lifetime (MG_NO_ALIAS=1: not)
+  size_t grad_bytes_unaliased = 0, grad_bytes = 0;   // gradient storage without / with sharing
   // schedule bookkeeping
   std::vector<Site> sites;
   // update of each node's parameters on a second stream, overlapping the rest
@@ -671,6 +674,82 @@ mg_status compile(mg_plan* p, const mg_graph_desc* d) {
   return MG_OK;
 }
 
+// Gradient buffers share storage when their lifetimes do not overlap (the
+// README's buffer-lifetime aliasing).  Positions along the step: the loss is
+// 0, the backward of node ni is 1 + (N - 1 - ni).  The gradient of value v is
+// written by the loss (the final value) or by the backward of v's consumer;
+// it is read by the backward of v's producer, and by the backward that forms
+// the gradient of the value whose skip connection ends at v (its dadd term).
+// A bias-gradient column sum reads it on the optimizer stream, after the
+// fact, so such a buffer is never shared.  Two buffers share a slot only if
+// one's last read comes strictly before the other's first write.
+void plan_gradients(mg_plan* p, Bump& b) {
+  const size_t es = dtype_size(p->dt);
+  const size_t B = (size_t)p->batch;
+  const int N = (int)p->nodes.size();
+  constexpr int kForever = 1 << 30;
+  auto pos = [&](int ni) { return 1 + (N - 1 - ni); };
+  struct Buf {
+    int v, start, end;
+    size_t bytes;
+  };
+  std::vector<Buf> bufs;
+  for (size_t vi = 1; vi < p->values.size(); ++vi) {
+    Value& v = p->values[vi];
+    if (!v.need_grad) continue;
+    v.has_grad = true;
+    Buf f{(int)vi, 0, 0, B * v.width * es};
+    if ((int)vi != p->final_value) {
+      f.start = kForever;
+      for (int ni = 0; ni < N; ++ni)
+        if (p->nodes[ni].in == (int)vi) f.start = std::min(f.start, pos(ni));
+    }
+    f.end = f.start;
+    if (v.producer >= 0) {
+      const Node& pr = p->nodes[v.producer];
+      f.end = std::max(f.end, pos(v.producer));
+      if (pr.kind == NK_LINEAR && pr.has_bias) f.end = kForever;
+    }
+    for (int ni = 0; ni < N; ++ni)
+      if (p->values[p->nodes[ni].in].pending_add == (int)vi) f.end = std::max(f.end, pos(ni));
+    bufs.push_back(f);
+    p->grad_bytes_unaliased += f.bytes;
+  }
+  std::stable_sort(bufs.begin(), bufs.end(), [](const Buf& a, const Buf& c) { return a.start < c.start; });
+  struct Slot {
+    size_t bytes;
+    int busy_until;
+    std::vector<int> members;
+  };
+  std::vector<Slot> slots;
+  for (const Buf& f : bufs) {
+    int pick = -1;
+    if (p->alias) {
+      // the smallest free slot that holds it, else the largest free slot (grown)
+      for (size_t k = 0; k < slots.size(); ++k) {
+        if (slots[k].busy_until >= f.start) continue;
+        if (slots[k].bytes >= f.bytes) {
+          if (pick < 0 || slots[pick].bytes < f.bytes || slots[k].bytes < slots[pick].bytes) pick = (int)k;
+        } else if (pick < 0 || (slots[pick].bytes < f.bytes && slots[k].bytes > slots[pick].bytes)) {
+          pick = (int)k;
+        }
+      }
+    }
+    if (pick < 0) {
+      slots.push_back(Slot{f.bytes, f.end, {f.v}});
+      continue;
+    }
+    slots[pick].bytes = std::max(slots[pick].bytes, f.bytes);
+    slots[pick].busy_until = f.end;
+    slots[pick].members.push_back(f.v);
+  }
+  for (const Slot& sl : slots) {
+    const size_t off = b.take(sl.bytes);
+    for (int vi : sl.members) p->values[vi].goff = off;
+    p->grad_bytes += sl.bytes;
+  }
+}
+
 void layout_workspace(mg_plan* p) {
   Bump b;
   const size_t es = dtype_size(p->dt);
@@ -678,11 +757,8 @@ void layout_workspace(mg_plan* p) {
   for (size_t i = 1; i < p->values.size(); ++i) {
     Value& v = p->values[i];
     v.off = b.take(B * v.width * es);
-    if (v.need_grad) {
-      v.goff = b.take(B * v.width * es);
-      v.has_grad = true;
-    }
   }
+  plan_gradients(p, b);
   // x's gradient is never formed; a value's need_grad is false for x
   for (Node& n : p->nodes) {
     if (n.kind == NK_RMSNORM) n.rstd_off = b.take(B * 4);
@@ -739,6 +815,9 @@ void build_dump(mg_plan* p) {
            : p->optimizer == MG_OPT_SGD    ? "sgd"
                                            : "sgd_momentum",
            p->loss, p->n_params, p->ws_bytes);
+  s += b;
+  snprintf(b, sizeof b, "  gradient storage: %zu bytes (%zu without lifetime sharing%s)\n",
+           p->grad_bytes, p->grad_bytes_unaliased, p->alias ? "" : "; MG_NO_ALIAS set");
   s += b;
   for (size_t i = 0; i < p->p_off.size(); ++i) {
     snprintf(b, sizeof b, "  param %zu: offset %zu [%d x %d]\n", i, p->p_off[i], p->p_rows[i],
@@ -801,6 +880,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     p->use_tc = strcmp(ev, "simt") != 0;
     p->use_pair = p->use_tc && strcmp(ev, "tc1") != 0;
   }
+  if (const char* ev = getenv("MG_NO_ALIAS")) p->alias = !(ev[0] == '1' && ev[1] == 0);
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
   if (e != cudaSuccess) {
