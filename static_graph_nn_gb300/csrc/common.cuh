@@ -78,4 +78,38 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return warp_max(t);
 }
 
+
+// Running softmax partial over 32 accumulator values of a row at columns n0..
+// (those below g.N), each taken as it will be stored (plus the bias, rounded
+// to the output type), kept in base 2: pm = max of x log2(e), ps = sum of
+// 2^(x log2(e) - pm).  For GEMM outputs with no activation, residual or saved
+// value.
+__device__ __forceinline__ void softmax_partial32(const GemmArgs& g, int n0, const float (&v)[32],
+                                                  float& pm, float& ps) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  float x[32];
+  float cm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    float t = v[j] + (g.bias && n < g.N ? g.bias[n] : 0.0f);
+    if (g.out_type == DT_BF16) t = __bfloat162float(__float2bfloat16_rn(t));
+    x[j] = n < g.N ? t * kLog2e : -INFINITY;
+    cm = fmaxf(cm, x[j]);
+  }
+  if (cm == -INFINITY) return;
+  if (cm > pm) {
+    ps = (pm == -INFINITY) ? 0.0f : ps * exp2f(pm - cm);
+    pm = cm;
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x[j] - pm));
+    acc += e;
+  }
+  ps += acc;
+}
+
 }  // namespace mg

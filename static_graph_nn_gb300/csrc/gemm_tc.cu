@@ -299,17 +299,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int m0 = (tile / P.tiles_n) * TC_BM, n0 = (tile % P.tiles_n) * BN;
       const int m = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      static_assert(BN == 256, "softmax partials cover 128 columns per epilogue warp");
+      float pm = -INFINITY, ps = 0.0f;             // softmax partial of this row's 128 columns
 #pragma unroll 1
       for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         if (m < P.g.M && n0 + c * 32 < P.g.N) {
-          if (P.splits > 1)
+          if (P.splits > 1) {
             split_add_row32(P.g, P.vec != 0, m, n0 + c * 32, v);
-          else
+          } else {
+            if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
             epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+          }
         }
       }
+      if (P.g.lse_part && m < P.g.M && n0 + half * (BN / 2) < P.g.N)
+        P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (BN / 2)) / 128] = make_float2(pm, ps);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }

@@ -331,12 +331,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const int n0 = (tile % P.tiles_n) * P_BN;
       const int m = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * P_BN);
+      float pm = -INFINITY, ps = 0.0f;             // softmax partial of this row's 128 columns
 #pragma unroll 1
       for (int c = half * (P_BN / 64); c < (half + 1) * (P_BN / 64); ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        if (m < P.g.M && n0 + c * 32 < P.g.N) epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+        if (m < P.g.M && n0 + c * 32 < P.g.N) {
+          if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
+          epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+        }
       }
+      if (P.g.lse_part && m < P.g.M && n0 + half * (P_BN / 2) < P.g.N)
+        P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (P_BN / 2)) / 128] = make_float2(pm, ps);
       tc_fence_before();
       mbar_arrive_remote(leader_tempty[acc]);
     }

@@ -29,6 +29,12 @@ struct GemmArgs {
   DType aux_type = DT_F32;   // dtype of out_z, saved, resid
   void* out = nullptr; long long ldo = 0;
   DType out_type = DT_F32;
+  // Softmax partials of the stored outputs (tcgen05 kernels; outputs with no
+  // activation, residual or saved value): for row m and 128-column chunk k,
+  // lse_part[m * lse_ld + k] = (max of y, sum of 2^(y - max)) over the chunk's
+  // columns below N, y = x log2(e), x the value as stored (bias added, rounded
+  // to out_type).
+  float2* lse_part = nullptr; int lse_ld = 0;
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
@@ -42,6 +48,14 @@ bool gemm_pair_eligible(const GemmArgs& g);
 cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s);
 
 // ---- loss ------------------------------------------------------------------
+// Softmax cross-entropy from logits whose per-row softmax partials the head
+// GEMM already wrote (GemmArgs::lse_part, nparts = ceil(C / 128) per row):
+// combines them into log-sum-exp, then one pass writes dlogits and the row
+// losses exactly as ce_loss does.  bf16 logits, C % 8 == 0.
+cudaError_t ce_loss_from_partials(const void* logits, int B, int C, long long ld,
+                                  const float2* parts, int nparts, int label_kind,
+                                  const void* labels, void* dlogits, float* row_loss,
+                                  float* loss, cudaStream_t s);
 // Softmax cross-entropy over rows of logits[B, C] (stride ld).  label_kind 0:
 // dense fp32 labels [B, C]; 1: int32 class ids [B].  Writes dlogits (same
 // dtype and layout as logits) = (p * sum(y) - y) / B, and row_loss[B] =

@@ -81,48 +81,13 @@ __global__ void __launch_bounds__(256) ce_kernel(const T* logits, int C, long lo
   }
 }
 
-// bf16 logits whose rows are whole 16-byte vectors (C % 8 == 0): the same two
-// passes with 8 columns per access.
+// The gradient pass of a bf16 row given its log-sum-exp: dense labels' sums,
+// dlogits = (softmax * sum(y) - y) / B, the row's loss.
 template <bool DENSE>
-__global__ void __launch_bounds__(256) ce_kernel_vec(const bf16* logits, int C, long long ld,
-                                                     const void* labels, bf16* dlogits,
-                                                     float* row_loss, float inv_b) {
-  __shared__ float red[32];
-  __shared__ float sh_m, sh_s;
-  const int r = blockIdx.x;
-  const bf16* z = logits + (size_t)r * ld;
-  bf16* dz = dlogits + (size_t)r * ld;
+__device__ __forceinline__ void ce_vec_tail(const bf16* z, bf16* dz, int C, const void* labels,
+                                            int r, float lse, float* red, float* row_loss,
+                                            float inv_b) {
   const int nv = C >> 3;
-  float m = -INFINITY, s = 0.0f;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    uint4 u = reinterpret_cast<const uint4*>(z)[v];
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 t = __bfloat1622float2(h[i]);
-      x[2 * i] = t.x;
-      x[2 * i + 1] = t.y;
-    }
-    float vm = x[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) vm = fmaxf(vm, x[i]);
-    if (vm > m) {
-      s = (m == -INFINITY) ? 0.0f : s * expf(m - vm);
-      m = vm;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s += expf(x[i] - m);
-  }
-  float bm = block_max(m, red);
-  float sc = (m == -INFINITY) ? 0.0f : s * expf(m - bm);
-  float bs = block_sum(sc, red);
-  if (threadIdx.x == 0) {
-    sh_m = bm;
-    sh_s = bs;
-  }
-  __syncthreads();
-  const float lse = sh_m + logf(sh_s);
   float ysum = 1.0f, yz = 0.0f;
   int t = -1;
   const float* y = DENSE ? static_cast<const float*>(labels) + (size_t)r * C : nullptr;
@@ -181,6 +146,83 @@ __global__ void __launch_bounds__(256) ce_kernel_vec(const bf16* logits, int C, 
   }
 }
 
+// bf16 logits whose rows are whole 16-byte vectors (C % 8 == 0): the same two
+// passes with 8 columns per access.
+template <bool DENSE>
+__global__ void __launch_bounds__(256) ce_kernel_vec(const bf16* logits, int C, long long ld,
+                                                     const void* labels, bf16* dlogits,
+                                                     float* row_loss, float inv_b) {
+  __shared__ float red[32];
+  __shared__ float sh_m, sh_s;
+  const int r = blockIdx.x;
+  const bf16* z = logits + (size_t)r * ld;
+  bf16* dz = dlogits + (size_t)r * ld;
+  const int nv = C >> 3;
+  float m = -INFINITY, s = 0.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    uint4 u = reinterpret_cast<const uint4*>(z)[v];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      x[2 * i] = t.x;
+      x[2 * i + 1] = t.y;
+    }
+    float vm = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) vm = fmaxf(vm, x[i]);
+    if (vm > m) {
+      s = (m == -INFINITY) ? 0.0f : s * expf(m - vm);
+      m = vm;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += expf(x[i] - m);
+  }
+  float bm = block_max(m, red);
+  float sc = (m == -INFINITY) ? 0.0f : s * expf(m - bm);
+  float bs = block_sum(sc, red);
+  if (threadIdx.x == 0) {
+    sh_m = bm;
+    sh_s = bs;
+  }
+  __syncthreads();
+  const float lse = sh_m + logf(sh_s);
+  ce_vec_tail<DENSE>(z, dz, C, labels, r, lse, red, row_loss, inv_b);
+}
+
+// Same from per-row softmax partials written by the head GEMM's epilogue (in
+// base 2: max of x log2 e and the sum of 2^(x log2 e - max), per 128-column
+// chunk), combined into the log-sum-exp, then the gradient pass.
+template <bool DENSE>
+__global__ void __launch_bounds__(256) ce_kernel_part(const bf16* logits, int C, long long ld,
+                                                      const float2* parts, int nparts,
+                                                      const void* labels, bf16* dlogits,
+                                                      float* row_loss, float inv_b) {
+  __shared__ float red[32];
+  __shared__ float sh_m, sh_s;
+  const int r = blockIdx.x;
+  // partials in base 2: (max of x log2 e, sum of 2^(x log2 e - max))
+  const float2* pr = parts + (size_t)r * nparts;
+  float m = -INFINITY;
+  for (int k = threadIdx.x; k < nparts; k += blockDim.x) m = fmaxf(m, pr[k].x);
+  const float bm = block_max(m, red);
+  float s = 0.0f;
+  for (int k = threadIdx.x; k < nparts; k += blockDim.x) {
+    const float2 q = pr[k];
+    if (q.x > -INFINITY) s += q.y * exp2f(q.x - bm);
+  }
+  const float bs = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    sh_m = bm;
+    sh_s = bs;
+  }
+  __syncthreads();
+  const float lse = (sh_m + log2f(sh_s)) * 0.6931471805599453f;   // back to base e
+  ce_vec_tail<DENSE>(logits + (size_t)r * ld, dlogits + (size_t)r * ld, C, labels, r, lse, red,
+                     row_loss, inv_b);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) mse_kernel(const T* o, const T* t, size_t n, T* dout,
                                                   float* partials, float two_over_n) {
@@ -227,6 +269,26 @@ cudaError_t ce_loss(DType t, const void* logits, int B, int C, long long ld, int
       ce_kernel<bf16, false><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, labels,
                                                (bf16*)dlogits, row_loss, inv_b);
   }
+  reduce_sum_kernel<<<1, 1024, 0, s>>>(row_loss, B, inv_b, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t ce_loss_from_partials(const void* logits, int B, int C, long long ld,
+                                  const float2* parts, int nparts, int label_kind,
+                                  const void* labels, void* dlogits, float* row_loss,
+                                  float* loss, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  if (C % 8 || ld % 8 || (reinterpret_cast<uintptr_t>(logits) & 15) ||
+      (reinterpret_cast<uintptr_t>(dlogits) & 15) ||
+      (label_kind == 0 && (reinterpret_cast<uintptr_t>(labels) & 15)) || nparts != (C + 127) / 128)
+    return cudaErrorInvalidValue;
+  const float inv_b = 1.0f / (float)B;
+  if (label_kind == 0)
+    ce_kernel_part<true><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, parts, nparts, labels,
+                                           (bf16*)dlogits, row_loss, inv_b);
+  else
+    ce_kernel_part<false><<<B, 256, 0, s>>>((const bf16*)logits, C, ld, parts, nparts, labels,
+                                            (bf16*)dlogits, row_loss, inv_b);
   reduce_sum_kernel<<<1, 1024, 0, s>>>(row_loss, B, inv_b, loss);
   return cudaGetLastError();
 }

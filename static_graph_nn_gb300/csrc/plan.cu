@@ -102,7 +102,8 @@ struct mg_plan {
   size_t ws_bytes = 0;
   char* ws = nullptr;
   size_t shadow_off = 0, chunks_off = 0, loss_off = 0, rowloss_off = 0, partial_off = 0,
-         colsum_off = 0, flag_off = 0;
+         colsum_off = 0, flag_off = 0, lse_part_off = 0;
+  int lse_parts = 0;         // 128-column softmax partials per logits row (0: not planned)
   int n_chunks = 0;
   const float* last_params = nullptr;
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
@@ -172,6 +173,7 @@ struct Exec {
   float* v = nullptr;
   float lr = 0.f;
   int step = 1;
+  bool ce_parts = false;   // the head GEMM wrote the logits' softmax partials
 };
 
 template <class F>
@@ -274,6 +276,14 @@ void forward_pass(Exec& e, const float* params, const void* x) {
       if (n.skip >= 0) { g.resid = val_ptr(p, n.skip, x); g.ldr = n.d_out; }
       g.aux_type = dt;
       g.out = p->ws + p->values[n.out].off; g.ldo = n.d_out; g.out_type = dt;
+      // the logits' softmax partials come out of the head GEMM's epilogue
+      // (tensor-core path only), so the loss reads the logits once
+      if (n.out == p->final_value && p->lse_parts && n.act == 0 && n.skip < 0 && n.in != 0 &&
+          tc_path(p, g)) {
+        g.lse_part = wsp<float2>(p, p->lse_part_off);
+        g.lse_ld = p->lse_parts;
+        e.ce_parts = true;
+      }
       site(e, gemm_name(p, "fwd", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
            [&] { return run_gemm(p, g, e.s); });
     } else if (n.kind == NK_RMSNORM) {
@@ -322,11 +332,20 @@ void loss_pass(Exec& e, const void* labels) {
     int kind = p->loss == MG_LOSS_CE_DENSE ? 0 : 1;
     double bytes = 2.0 * dtype_size(dt) * B * C + (kind == 0 ? 4.0 * B * C : 4.0 * B);
     char nm[96];
-    snprintf(nm, sizeof nm, "softmax_ce_%s %dx%d", kind == 0 ? "dense" : "index", B, C);
-    site(e, nm, 0, bytes, 2, [&] {
-      return ce_loss(dt, logits, B, C, C, kind, labels, dlogits, wsp<float>(p, p->rowloss_off),
-                     wsp<float>(p, p->loss_off), e.s);
-    });
+    if (e.ce_parts) {
+      snprintf(nm, sizeof nm, "softmax_ce_%s %dx%d (GEMM partials)", kind == 0 ? "dense" : "index", B, C);
+      site(e, nm, 0, bytes + 8.0 * B * p->lse_parts, 2, [&] {
+        return ce_loss_from_partials(logits, B, C, C, wsp<float2>(p, p->lse_part_off), p->lse_parts,
+                                     kind, labels, dlogits, wsp<float>(p, p->rowloss_off),
+                                     wsp<float>(p, p->loss_off), e.s);
+      });
+    } else {
+      snprintf(nm, sizeof nm, "softmax_ce_%s %dx%d", kind == 0 ? "dense" : "index", B, C);
+      site(e, nm, 0, bytes, 2, [&] {
+        return ce_loss(dt, logits, B, C, C, kind, labels, dlogits, wsp<float>(p, p->rowloss_off),
+                       wsp<float>(p, p->loss_off), e.s);
+      });
+    }
   }
 }
 
@@ -784,6 +803,13 @@ void layout_workspace(mg_plan* p) {
   if (part < (size_t)kMsePartials * 4) part = (size_t)kMsePartials * 4;
   p->partial_off = b.take(part);
   p->colsum_off = b.take(kColsumFloats * 4);   // the bias-gradient sums' own partials (aux stream)
+  // softmax partials of a cross-entropy head computed by a tensor-core GEMM
+  const Value& fv = p->values[p->final_value];
+  if (p->dt == DT_BF16 && p->loss != MG_LOSS_MSE && fv.width % 8 == 0 && fv.producer >= 0 &&
+      p->nodes[fv.producer].kind == NK_LINEAR) {
+    p->lse_parts = (fv.width + 127) / 128;
+    p->lse_part_off = b.take(B * (size_t)p->lse_parts * sizeof(float2));
+  }
   p->ws_bytes = round_up(b.top, kWsAlign);
 }
 
