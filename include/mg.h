@@ -145,6 +145,15 @@ mg_status mg_train_step(mg_plan* plan, float* params, float* grads, float* adam_
 /* Copy the last step's loss to the host; synchronises `stream`. */
 mg_status mg_loss(mg_plan* plan, float* host_loss, mg_stream_t stream);
 
+/* Enqueue, without waiting, a copy of the last step's loss and the plan's
+ * pipeline error word to host memory: host_dst receives { float loss; int
+ * timed_out; } (8 bytes; pinned memory keeps the copy asynchronous).  The
+ * values are valid once `stream` has passed this point (an event, a later
+ * synchronisation).  A nonzero timed_out means that step's results are
+ * invalid; mg_loss reports it as MG_ERR_TIMEOUT and clears it.  For training
+ * loops that enqueue the next step before reading this one's loss. */
+mg_status mg_loss_async(mg_plan* plan, void* host_dst, mg_stream_t stream);
+
 /* Device address of the last step's loss (one fp32), valid until destroy. */
 const float* mg_loss_device_ptr(const mg_plan* plan);
 

@@ -52,6 +52,7 @@ _SIGS = {
     "mg_train_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, ctypes.c_int, _P]),
     "mg_loss": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float), _P]),
     "mg_loss_device_ptr": (_P, [_P]),
+    "mg_loss_async": (ctypes.c_int, [_P, ctypes.c_void_p, _P]),
     "mg_refresh_params": (ctypes.c_int, [_P, _P, _P]),
     "mg_plan_dump": (ctypes.c_size_t, [_P, ctypes.c_char_p, ctypes.c_size_t]),
     "mg_last_error": (ctypes.c_char_p, [_P]),
@@ -200,6 +201,11 @@ class Plan:
         v = ctypes.c_float()
         self._check(self.lib.mg_loss(self.h, ctypes.byref(v), _stream(stream)))
         return v.value
+
+    def loss_async(self, host_dst, stream=None):
+        """Enqueue the copy of this step's (loss, timed_out) pair into 8 bytes of
+        host memory (a pinned tensor or an address); no wait."""
+        self._check(self.lib.mg_loss_async(self.h, _ptr(host_dst), _stream(stream)))
 
     def loss_device_ptr(self) -> int:
         return self.lib.mg_loss_device_ptr(self.h)

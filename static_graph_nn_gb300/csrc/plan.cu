@@ -1055,6 +1055,14 @@ mg_status mg_loss(mg_plan* p, float* host_loss, mg_stream_t stream) {
   return MG_OK;
 }
 
+mg_status mg_loss_async(mg_plan* p, void* host_dst, mg_stream_t stream) {
+  if (!p || !host_dst) return fail(p, MG_ERR_INVALID_ARG, "plan and host_dst must be non-NULL");
+  cudaError_t e = cudaMemcpyAsync(host_dst, p->ws + p->loss_off, 8, cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "mg_loss_async");
+  return MG_OK;
+}
+
 const float* mg_loss_device_ptr(const mg_plan* p) {
   return p ? reinterpret_cast<const float*>(p->ws + p->loss_off) : nullptr;
 }
