@@ -919,7 +919,11 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
   std::vector<Chunk> ch = chunk_table(p);
   e = cudaMemcpy(p->ws + p->chunks_off, ch.data(), ch.size() * sizeof(Chunk), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->ws + p->loss_off, 0, 16);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->aux, cudaStreamNonBlocking);
+  // the optimizer stream gets the lowest priority: when a backward GEMM and
+  // optimizer blocks wait for SMs together, the GEMM's CTAs go first
+  int prio_lo = 0, prio_hi = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->aux, cudaStreamNonBlocking, prio_lo);
   p->node_ev.assign(2 * p->nodes.size(), nullptr);   // per node: updates, bias-gradient sum
   for (auto& ev : p->node_ev)
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
