@@ -111,17 +111,27 @@ __device__ __forceinline__ void st8(bf16* p, const float* f) {
   *reinterpret_cast<uint4*>(p) = u;
 }
 
+// NV = vectors per thread (d <= 2048 NV for 256 threads); gamma stays in
+// registers across the rows a block visits.
+template <int NV>
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_vec(const bf16* x, const float* gamma,
                                                                 bf16* y, float* rstd, int rows,
                                                                 int d, float eps) {
   __shared__ float red[32];
   const int nvec = d >> 3;
+  float gm[NV][8];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int vi = threadIdx.x + i * NORM_THREADS;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) gm[i][j] = vi < nvec ? gamma[vi * 8 + j] : 0.0f;
+  }
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const bf16* xr = x + (size_t)r * d;
-    float v[NV_MAX][8];
+    float v[NV][8];
     float ss = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NV_MAX; ++i) {
+    for (int i = 0; i < NV; ++i) {
       int vi = threadIdx.x + i * NORM_THREADS;
       if (vi < nvec) {
         ld8(xr + vi * 8, v[i]);
@@ -134,18 +144,19 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_fwd_vec(const bf16* x, c
     if (threadIdx.x == 0) rstd[r] = rs;
     bf16* yr = y + (size_t)r * d;
 #pragma unroll
-    for (int i = 0; i < NV_MAX; ++i) {
+    for (int i = 0; i < NV; ++i) {
       int vi = threadIdx.x + i * NORM_THREADS;
       if (vi < nvec) {
         float o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = v[i][j] * rs * gamma[vi * 8 + j];
+        for (int j = 0; j < 8; ++j) o[j] = v[i][j] * rs * gm[i][j];
         st8(yr + vi * 8, o);
       }
     }
   }
 }
 
+template <int NV>
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, const bf16* x,
                                                                 const float* rstd,
                                                                 const float* gamma,
@@ -154,17 +165,22 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, 
                                                                 int d) {
   __shared__ float red[32];
   const int nvec = d >> 3;
-  float dg[NV_MAX][8];
+  float dg[NV][8], gm[NV][8];
 #pragma unroll
-  for (int i = 0; i < NV_MAX; ++i)
+  for (int i = 0; i < NV; ++i) {
+    const int vi = threadIdx.x + i * NORM_THREADS;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dg[i][j] = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+      dg[i][j] = 0.0f;
+      gm[i][j] = vi < nvec ? gamma[vi * 8 + j] : 0.0f;
+    }
+  }
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const float rs = rstd[r];
-    float xv[NV_MAX][8], gv[NV_MAX][8];
+    float xv[NV][8], gv[NV][8];
     float gx = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NV_MAX; ++i) {
+    for (int i = 0; i < NV; ++i) {
       int vi = threadIdx.x + i * NORM_THREADS;
       if (vi < nvec) {
         float dyv[8];
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, 
         ld8(x + (size_t)r * d + vi * 8, xv[i]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          gv[i][j] = dyv[j] * gamma[vi * 8 + j];
+          gv[i][j] = dyv[j] * gm[i][j];
           dg[i][j] += dyv[j] * xv[i][j] * rs;
           gx += gv[i][j] * xv[i][j];
         }
@@ -182,7 +198,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, 
       gx = block_sum(gx, red) / (float)d;
       const float k = rs * rs * gx;
 #pragma unroll
-      for (int i = 0; i < NV_MAX; ++i) {
+      for (int i = 0; i < NV; ++i) {
         int vi = threadIdx.x + i * NORM_THREADS;
         if (vi < nvec) {
           float o[8], a[8];
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_bwd_vec(const bf16* dy, 
     }
   }
 #pragma unroll
-  for (int i = 0; i < NV_MAX; ++i) {
+  for (int i = 0; i < NV; ++i) {
     int vi = threadIdx.x + i * NORM_THREADS;
     if (vi < nvec) {
 #pragma unroll
@@ -313,7 +329,13 @@ cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, flo
   int grid = rows < 152 * 16 ? rows : 152 * 16;
   if (t == DT_BF16 && d % 8 == 0 && d <= NORM_THREADS * 8 * NV_MAX &&
       (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
-    rmsnorm_fwd_vec<<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd, rows, d, eps);
+    const int nv = (d / 8 + NORM_THREADS - 1) / NORM_THREADS;
+    if (nv == 1)
+      rmsnorm_fwd_vec<1><<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd, rows, d, eps);
+    else if (nv == 2)
+      rmsnorm_fwd_vec<2><<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd, rows, d, eps);
+    else
+      rmsnorm_fwd_vec<NV_MAX><<<grid, NORM_THREADS, 0, s>>>((const bf16*)x, gamma, (bf16*)y, rstd, rows, d, eps);
     return cudaGetLastError();
   }
   if (t == DT_F32)
@@ -332,9 +354,17 @@ cudaError_t rmsnorm_bwd(DType t, const void* dy, const void* x, const float* rst
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   if (t == DT_BF16 && d % 8 == 0 && d <= NORM_THREADS * 8 * NV_MAX && al(dy) && al(x) &&
       al(dadd) && al(dx)) {
-    rmsnorm_bwd_vec<<<row_chunks, NORM_THREADS, 0, s>>>((const bf16*)dy, (const bf16*)x, rstd,
-                                                        gamma, (const bf16*)dadd, (bf16*)dx,
-                                                        dgamma_partials, rows, d);
+    const int nv = (d / 8 + NORM_THREADS - 1) / NORM_THREADS;
+    auto kern = nv == 1 ? rmsnorm_bwd_vec<1> : nv == 2 ? rmsnorm_bwd_vec<2> : rmsnorm_bwd_vec<NV_MAX>;
+    // one wave: as many blocks as can be resident at once (at most row_chunks)
+    int occ = 0, dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NORM_THREADS, 0) == cudaSuccess &&
+        occ > 0 && occ * sms < row_chunks)
+      row_chunks = occ * sms;
+    kern<<<row_chunks, NORM_THREADS, 0, s>>>((const bf16*)dy, (const bf16*)x, rstd, gamma,
+                                             (const bf16*)dadd, (bf16*)dx, dgamma_partials, rows, d);
     colsum_pass2_wide<<<(d + 31) / 32, 256, 0, s>>>(dgamma_partials, row_chunks, d, dgamma);
     return cudaGetLastError();
   }

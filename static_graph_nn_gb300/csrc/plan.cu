@@ -36,7 +36,7 @@ std::string g_err = "";
 constexpr size_t kAlignElems = 64;      // parameter offsets (256 B in fp32)
 constexpr size_t kWsAlign = 1024;       // workspace region alignment
 constexpr int kChunk = 16384;           // optimizer chunk (elements)
-constexpr int kNormChunks = 4 * 152;    // RMSNorm backward blocks (dgamma partial rows)
+constexpr int kNormChunks = 8 * 152;    // RMSNorm backward blocks (dgamma partial rows)
 constexpr int kMsePartials = 1024;
 constexpr size_t kColsumFloats = (size_t)kColsumBlocks * 2048;   // column-sum partials capacity
 
