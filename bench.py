@@ -341,16 +341,17 @@ def main():
         one_step()
     torch.cuda.synchronize()
 
-    # ---- timed region: device-resident inputs, per-kernel events ----
+    # ---- timed region: device-resident inputs, the steps as a user runs
+    # them (from the second call on, each step is a CUDA-graph replay) ----
     try:
         clocks = NvmlSampler(local)
     except Exception:
         clocks = ClockSampler(local)
     clocks.start()
-    plan.profile_begin(args.steps)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    replays0 = plan.graph_replays()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -361,9 +362,22 @@ def main():
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
+    launches = plan.last_launch_count() * args.steps
+    replays = plan.graph_replays() - replays0
+
+    # ---- kernel timing: the same K steps again, launched directly with a
+    # CUDA event pair around every kernel on the stream it runs on ----
+    plan.profile_begin(args.steps)
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    ev3.record(stream)
+    torch.cuda.synchronize()
+    ms_prof = ev2.elapsed_time(ev3)
     prof = plan.profile_end()
     clk = clocks.stop()
-    launches = plan.last_launch_count() * args.steps
     loss = plan.loss(stream)
 
     # ---- end to end: host buffers, H2D copies and the loss read inside ----
@@ -373,14 +387,16 @@ def main():
     # the pipeline's error flag) is copied back and read on the host one step
     # later, so the copies overlap the compute and the host enqueues the next
     # step while the GPU runs this one.
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(10, args.steps)
+    e2e_warm = max(4, args.warmup)
+    total = e2e_warm + e2e_steps
     copy_stream = torch.cuda.Stream()
     xb = [x_dev, torch.empty_like(x_dev)]
     yb = [y_dev, torch.empty_like(y_dev)]
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
-    done = [torch.cuda.Event() for _ in range(e2e_steps)]
-    loss_host = torch.zeros(e2e_steps, 2, dtype=torch.float32).pin_memory()
+    done = [torch.cuda.Event() for _ in range(total)]
+    loss_host = torch.zeros(total, 2, dtype=torch.float32).pin_memory()
     e2e_losses = []
 
     # inputs under 1 MiB are copied on the compute stream itself: their copy is
@@ -399,13 +415,19 @@ def main():
             yb[b].copy_(y_host, non_blocking=True)
             copied[b].record(copy_stream)
 
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    t0 = time.perf_counter()
+    # the loop's first e2e_warm steps are untimed warm-up (each buffer's step
+    # graph is captured on its second use); the clock starts at the step after
+    # (that step's input copy is enqueued after the clock starts)
+    t0 = None
     enqueue_copy(0)
-    for t in range(e2e_steps):
-        if t + 1 < e2e_steps:
+    for t in range(total):
+        if t == e2e_warm:
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            enqueue_copy(t)
+        if t + 1 < total and t + 1 != e2e_warm:
             enqueue_copy(t + 1)
         b = t & 1
         if overlap:
@@ -419,11 +441,11 @@ def main():
             consumed[b].record(stream)
         plan.loss_async(loss_host[t].data_ptr(), stream)
         done[t].record(stream)
-        if t > 0:
+        if t > e2e_warm:
             done[t - 1].synchronize()
             e2e_losses.append(float(loss_host[t - 1, 0]))
-    done[e2e_steps - 1].synchronize()
-    e2e_losses.append(float(loss_host[e2e_steps - 1, 0]))
+    done[total - 1].synchronize()
+    e2e_losses.append(float(loss_host[total - 1, 0]))
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     if any(loss_host.view(torch.int32)[:, 1].tolist()) or not all(map(math.isfinite, e2e_losses)):
         raise RuntimeError("end-to-end steps reported a timed-out pipeline or a non-finite loss")
@@ -497,6 +519,10 @@ def main():
                              "gbs": f["bytes"] / (f["total_ms"] * 1e-3) / 1e9 if f["total_ms"] else None}
                             for f in sorted(fam.values(), key=lambda f: -f["total_ms"])],
         "gpu_launches": launches,
+        "graph_replays_timed": replays,
+        "kernel_timing": {"steps": args.steps, "ms_per_step": ms_prof / args.steps,
+                          "how": "the K steps after the timed region, launched directly with a "
+                                 "CUDA event pair around every kernel (roofline and kernels)"},
         "loss": loss,
         "clocks": clk,
         "e2e": {"value": job_throughput(world, 1, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d,

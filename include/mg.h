@@ -137,7 +137,16 @@ mg_status mg_forward(mg_plan* plan, const float* params, const void* x, float* o
  * The loss of the step is kept on the device (mg_loss, mg_loss_device_ptr).
  * grads must not alias params.  The bf16 weight copy used by the bf16 path is
  * refreshed from params automatically when step == 1 or params differs from the
- * previous call; otherwise the previous update has kept it current. */
+ * previous call; otherwise the previous update has kept it current.
+ * Graph replay: the second call with the same six buffer addresses captures
+ * the step's launches (both streams) into a CUDA graph, and that call and
+ * later ones with those addresses launch the graph on `stream`, with lr and
+ * the bias corrections of `step` written into its optimizer nodes.  Graphs
+ * are kept for the two most recently used address sets (double-buffered
+ * inputs).  Results are the same as launching each kernel.  Not used while
+ * profiling or when `stream` is itself being captured; the environment
+ * variable MG_GRAPH=0, read at plan creation, turns it off.  If a capture
+ * fails the plan launches directly from then on. */
 mg_status mg_train_step(mg_plan* plan, float* params, float* grads, float* adam_m,
                         float* adam_v, const void* x, const void* labels, float lr, int step,
                         mg_stream_t stream);
@@ -203,8 +212,12 @@ const char* mg_last_error(const mg_plan* plan);
 mg_status mg_debug_check_finite(mg_plan* plan, const float* data, size_t n, long long* first_bad,
                                 mg_stream_t stream);
 
-/* Kernels launched by the last mg_train_step / mg_forward call. */
+/* Kernels launched by the last mg_train_step / mg_forward call (a replayed
+ * step counts the kernels its graph holds). */
 int mg_last_launch_count(const mg_plan* plan);
+
+/* mg_train_step calls served by a graph replay since the plan was created. */
+long long mg_graph_replays(const mg_plan* plan);
 
 /* ---- per-kernel timing (CUDA events around each launch) ----------------
  * mg_profile_begin(plan, max_calls): from now on, each mg_train_step records

@@ -59,6 +59,7 @@ _SIGS = {
     "mg_debug_check_finite": (ctypes.c_int, [_P, _P, ctypes.c_size_t,
                                              ctypes.POINTER(ctypes.c_longlong), _P]),
     "mg_last_launch_count": (ctypes.c_int, [_P]),
+    "mg_graph_replays": (ctypes.c_longlong, [_P]),
     "mg_profile_begin": (ctypes.c_int, [_P, ctypes.c_int]),
     "mg_profile_end": (ctypes.c_int, [_P]),
     "mg_profile_entries": (ctypes.c_int, [_P]),
@@ -246,6 +247,9 @@ class Plan:
 
     def last_launch_count(self) -> int:
         return self.lib.mg_last_launch_count(self.h)
+
+    def graph_replays(self) -> int:
+        return self.lib.mg_graph_replays(self.h)
 
     def profile_begin(self, max_calls: int):
         self._check(self.lib.mg_profile_begin(self.h, max_calls))

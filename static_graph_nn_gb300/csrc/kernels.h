@@ -109,6 +109,15 @@ struct Chunk {  // a run of one tensor's elements in the flat buffers
 cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
                         float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
                         float beta1, float beta2, float eps, cudaStream_t s);
+// The optimizer update kernels' argument layout, for replaying a captured
+// step with new step scalars: argument count and sizes, and the indices of
+// lr / (1 - b1^t), 1 / sqrt(1 - b2^t) (Adam, LaProp) or lr (SGD, momentum).
+struct OptKernelInfo {
+  int nargs;
+  int size[12];
+  int i_lr_bc1, i_inv_sqrt_bc2, i_lr;
+};
+bool optimizer_kernel_info(const void* func, OptKernelInfo* info);
 cudaError_t laprop_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
                           float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
                           float beta1, float beta2, float eps, cudaStream_t s);

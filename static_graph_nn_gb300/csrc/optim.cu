@@ -177,6 +177,36 @@ __global__ void nonfinite_kernel(const float* d, size_t n, unsigned long long* f
 
 }  // namespace
 
+bool optimizer_kernel_info(const void* func, OptKernelInfo* info) {
+  // argument lists of the update kernels above: pointers are 8 bytes, scalars 4
+  static const int two_moment[11] = {8, 8, 8, 8, 8, 8, 4, 4, 4, 4, 4};
+  static const int momentum[7] = {8, 8, 8, 8, 8, 4, 4};
+  static const int sgd[5] = {8, 8, 8, 8, 4};
+  const int* sizes = nullptr;
+  if (func == reinterpret_cast<const void*>(adam_kernel) ||
+      func == reinterpret_cast<const void*>(laprop_kernel)) {
+    sizes = two_moment;
+    info->nargs = 11;
+    info->i_lr_bc1 = 6;
+    info->i_inv_sqrt_bc2 = 7;
+    info->i_lr = -1;
+  } else if (func == reinterpret_cast<const void*>(momentum_kernel)) {
+    sizes = momentum;
+    info->nargs = 7;
+    info->i_lr_bc1 = info->i_inv_sqrt_bc2 = -1;
+    info->i_lr = 5;
+  } else if (func == reinterpret_cast<const void*>(sgd_kernel)) {
+    sizes = sgd;
+    info->nargs = 5;
+    info->i_lr_bc1 = info->i_inv_sqrt_bc2 = -1;
+    info->i_lr = 4;
+  } else {
+    return false;
+  }
+  for (int i = 0; i < info->nargs; ++i) info->size[i] = sizes[i];
+  return true;
+}
+
 cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
                         float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
                         float beta1, float beta2, float eps, cudaStream_t s) {

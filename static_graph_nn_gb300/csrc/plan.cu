@@ -109,6 +109,29 @@ struct mg_plan {
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
   bool use_pair = true;      // SM-pair GEMMs for large shapes (MG_GEMM=tc1 turns them off)
   bool alias = true;         // gradient buffers share storage by lifetime (MG_NO_ALIAS=1: not)
+  // CUDA-graph replay of the training step (MG_GRAPH=0: every kernel launched
+  // directly): a step is captured on the second call with the same buffers
+  // and relaunched with the optimizer nodes' step scalars updated; graphs for
+  // the two most recent buffer sets are kept (double-buffered inputs)
+  bool use_graph = true;
+  struct OptNode {
+    cudaGraphNode_t node;
+    cudaKernelNodeParams kp;
+    OptKernelInfo info;
+    uint64_t arg[12];
+    void* argv[12];
+  };
+  struct StepGraph {
+    const void* key[6] = {};
+    int calls = 0, launches = 0;
+    long long last_use = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t gexec = nullptr;
+    std::vector<OptNode> opt_nodes;
+  };
+  std::vector<StepGraph> graphs;
+  long long graph_clock = 0, graph_replays = 0;
+  cudaStream_t cap = nullptr;   // private stream the step is captured on
   size_t grad_bytes_unaliased = 0, grad_bytes = 0;   // gradient storage without / with sharing
   // schedule bookkeeping
   std::vector<Site> sites;
@@ -882,6 +905,125 @@ void mg::set_global_error(const char* msg) {
 }
 
 // ============================================================================
+namespace {
+
+void drop_graph(mg_plan::StepGraph& g) {
+  if (g.gexec) cudaGraphExecDestroy(g.gexec);
+  if (g.graph) cudaGraphDestroy(g.graph);
+  g.gexec = nullptr;
+  g.graph = nullptr;
+  g.opt_nodes.clear();
+}
+
+// The optimizer's step scalars as node_update computes them.
+void step_scalars(const mg_plan* p, float lr, int step, float* lr_bc1, float* inv_sqrt_bc2) {
+  double bc1 = 1.0 - std::pow((double)p->beta1, (double)step);
+  double bc2 = 1.0 - std::pow((double)p->beta2, (double)step);
+  *lr_bc1 = (float)(lr / bc1);
+  *inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+}
+
+// The graph entry for this buffer set (created, evicting the least recently
+// used of two, when new).
+mg_plan::StepGraph& graph_entry(mg_plan* p, const void* const (&key)[6]) {
+  ++p->graph_clock;
+  for (auto& g : p->graphs)
+    if (memcmp(g.key, key, sizeof g.key) == 0) {
+      g.last_use = p->graph_clock;
+      return g;
+    }
+  if (p->graphs.size() >= 2) {
+    size_t old = p->graphs[0].last_use <= p->graphs[1].last_use ? 0 : 1;
+    drop_graph(p->graphs[old]);
+    p->graphs.erase(p->graphs.begin() + old);
+  }
+  p->graphs.emplace_back();
+  mg_plan::StepGraph& g = p->graphs.back();
+  memcpy(g.key, key, sizeof g.key);
+  g.last_use = p->graph_clock;
+  return g;
+}
+
+// Capture one step into a graph; false (and nothing kept) if any part of the
+// capture fails.
+bool capture_step(mg_plan* p, mg_plan::StepGraph& sg, float* params, float* grads,
+                  float* m, float* v, const void* x, const void* labels, float lr, int step) {
+  // captured on a private stream (the caller's may be the legacy default
+  // stream, which cannot be captured); nothing runs during the capture
+  if (!p->cap && cudaStreamCreateWithFlags(&p->cap, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (cudaStreamBeginCapture(p->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  Exec ex{p, p->cap, false, false};
+  train_schedule(ex, params, grads, m, v, x, labels, lr, step);
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(p->cap, &g);
+  if (ex.err != cudaSuccess || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return false;
+  }
+  cudaGraphExec_t ge = nullptr;
+  if (cudaGraphInstantiate(&ge, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return false;
+  }
+  // the optimizer kernel nodes, with a copy of their arguments
+  size_t n = 0;
+  cudaGraphGetNodes(g, nullptr, &n);
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n) cudaGraphGetNodes(g, nodes.data(), &n);
+  sg.opt_nodes.clear();
+  for (cudaGraphNode_t nd : nodes) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nd, &t) != cudaSuccess || t != cudaGraphNodeTypeKernel) continue;
+    cudaKernelNodeParams kp;
+    if (cudaGraphKernelNodeGetParams(nd, &kp) != cudaSuccess) continue;
+    mg_plan::OptNode o;
+    if (!optimizer_kernel_info(kp.func, &o.info)) continue;
+    o.node = nd;
+    o.kp = kp;
+    for (int i = 0; i < o.info.nargs; ++i) {
+      o.arg[i] = 0;
+      memcpy(&o.arg[i], kp.kernelParams[i], o.info.size[i]);
+    }
+    sg.opt_nodes.push_back(o);
+  }
+  for (auto& o : sg.opt_nodes) {
+    for (int i = 0; i < o.info.nargs; ++i) o.argv[i] = &o.arg[i];
+    o.kp.kernelParams = o.argv;
+    o.kp.extra = nullptr;
+  }
+  sg.graph = g;
+  sg.gexec = ge;
+  sg.launches = ex.launches;
+  return true;
+}
+
+// Relaunch a captured step with this step's optimizer scalars.
+cudaError_t replay_step(mg_plan* p, mg_plan::StepGraph& sg, cudaStream_t s, float lr, int step) {
+  float lr_bc1 = lr, inv = 1.0f;
+  if (p->optimizer == MG_OPT_ADAM || p->optimizer == MG_OPT_LAPROP)
+    step_scalars(p, lr, step, &lr_bc1, &inv);
+  for (auto& o : sg.opt_nodes) {
+    if (o.info.i_lr_bc1 >= 0) memcpy(&o.arg[o.info.i_lr_bc1], &lr_bc1, 4);
+    if (o.info.i_inv_sqrt_bc2 >= 0) memcpy(&o.arg[o.info.i_inv_sqrt_bc2], &inv, 4);
+    if (o.info.i_lr >= 0) memcpy(&o.arg[o.info.i_lr], &lr, 4);
+    cudaError_t e = cudaGraphExecKernelNodeSetParams(sg.gexec, o.node, &o.kp);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaGraphLaunch(sg.gexec, s);
+  if (e == cudaSuccess) ++p->graph_replays;
+  return e;
+}
+
+}  // namespace
+
 extern "C" {
 
 mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
@@ -907,6 +1049,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     p->use_pair = p->use_tc && strcmp(ev, "tc1") != 0;
   }
   if (const char* ev = getenv("MG_NO_ALIAS")) p->alias = !(ev[0] == '1' && ev[1] == 0);
+  if (const char* ev = getenv("MG_GRAPH")) p->use_graph = !(ev[0] == '0' && ev[1] == 0);
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
   if (e != cudaSuccess) {
@@ -952,6 +1095,8 @@ void mg_step_plan_destroy(mg_plan* p) {
   cudaGetDevice(&prev);
   cudaSetDevice(p->device);
   cudaDeviceSynchronize();
+  for (auto& g : p->graphs) drop_graph(g);
+  if (p->cap) cudaStreamDestroy(p->cap);
   for (auto ev : p->events) cudaEventDestroy(ev);
   for (auto ev : p->node_ev)
     if (ev) cudaEventDestroy(ev);
@@ -1035,6 +1180,24 @@ mg_status mg_train_step(mg_plan* p, float* params, float* grads, float* adam_m, 
     extra = 1;
   }
   p->last_params = params;
+  // graph replay: the buffers of a captured step, no profiling, and the
+  // caller's stream not itself being captured
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (p->use_graph && !p->profiling && cs == cudaStreamCaptureStatusNone) {
+    const void* key[6] = {params, grads, adam_m, adam_v, x, labels};
+    mg_plan::StepGraph& sg = graph_entry(p, key);
+    ++sg.calls;
+    if (!sg.gexec && sg.calls >= 2 &&
+        !capture_step(p, sg, params, grads, adam_m, adam_v, x, labels, lr, step))
+      p->use_graph = false;   // capture unavailable here: launch directly from now on
+    if (sg.gexec) {
+      e = replay_step(p, sg, s, lr, step);
+      if (e != cudaSuccess) return cuda_fail(p, e, "mg_train_step graph launch");
+      p->last_launches = extra + sg.launches;
+      return MG_OK;
+    }
+  }
   Exec ex{p, s, false, true};
   ex.launches = extra;
   train_schedule(ex, params, grads, adam_m, adam_v, x, labels, lr, step);
@@ -1264,6 +1427,8 @@ mg_status mg_debug_check_finite(mg_plan* p, const float* data, size_t n, long lo
 }
 
 int mg_last_launch_count(const mg_plan* p) { return p ? p->last_launches : 0; }
+
+long long mg_graph_replays(const mg_plan* p) { return p ? p->graph_replays : 0; }
 
 mg_status mg_profile_begin(mg_plan* p, int max_calls) {
   if (!p || max_calls <= 0) return fail(p, MG_ERR_INVALID_ARG, "bad profile request");
