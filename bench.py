@@ -176,6 +176,8 @@ def kernel_family(site_name: str) -> str:
             return "gemm_tc_kernel (tcgen05)"
         if "f32-ffma" in n:
             return "gemm_simt (fp32 FFMA)"
+        if "skinny" in n:
+            return "gemm_skinny (bf16, narrow side in shared memory)"
         return "gemm_simt (bf16)"
     if n.startswith("attn_fwd"):
         return "attn_fwd" + (" (tcgen05)" if "tcgen05" in n else " (simt)")

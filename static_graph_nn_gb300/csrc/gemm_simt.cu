@@ -299,6 +299,341 @@ cudaError_t launch_dw_narrow(const GemmArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---- bf16 GEMMs with one narrow side (a head of a few classes) ------------
+// The narrow operand is held in shared memory as fp32; the wide one streams
+// through once.  Same epilogue arithmetic as above.
+
+int sm_count_simt() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+__device__ __forceinline__ void unpack8(const bf16* p, float (&f)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ void pack8(bf16* p, const float (&f)[8]) {
+  uint4 u;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+// epilogue_elem on eight consecutive outputs of row m (bf16 output and
+// auxiliaries) with 16-byte loads and stores.
+__device__ __forceinline__ void epilogue8_bf16(const GemmArgs& g, int m, int n0, float (&v)[8]) {
+  float sv[8], rs[8], z[8];
+  if (g.dact) unpack8(static_cast<const bf16*>(g.saved) + (size_t)m * g.lds + n0, sv);
+  if (g.resid) unpack8(static_cast<const bf16*>(g.resid) + (size_t)m * g.ldr + n0, rs);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float x = v[j];
+    if (g.bias) x += g.bias[n0 + j];
+    if (g.act || g.resid || g.out_z) x = round_value<bf16>(x);
+    z[j] = x;
+    if (g.act) x = apply_act(g.act, x);
+    if (g.dact) {
+      x = round_value<bf16>(x);
+      x *= act_grad_from_saved(g.dact, sv[j]);
+    }
+    if (g.resid) x += rs[j];
+    v[j] = x;
+  }
+  if (g.out_z) pack8(static_cast<bf16*>(g.out_z) + (size_t)m * g.ldz + n0, z);
+  pack8(static_cast<bf16*>(g.out) + (size_t)m * g.ldo + n0, v);
+}
+
+// Forward, N <= NP: out[m][n] = sum_k A[m][k] B[k][n] (A K-major, B N-major).
+// B is held transposed in shared memory ([NP][ks], zero padded to k2, a
+// multiple of 64).  A warp owns R rows at a time; lane l takes the bf16 pairs
+// at k = 2l + 64i of each row; the partial sums are reduced across the warp
+// and lane n applies the epilogue to column n.
+template <int NP, int R, typename TO>
+__global__ void __launch_bounds__(256) skinny_fwd_kernel(const GemmArgs g, int k2, int vec2) {
+  extern __shared__ __align__(16) float sbt[];
+  const int ks = k2 + 2;   // row stride: float2-aligned, rows two banks apart
+  const bf16* B = static_cast<const bf16*>(g.B);
+  for (int i = threadIdx.x; i < k2 * NP; i += blockDim.x) {
+    const int k = i / NP, n = i - k * NP;
+    sbt[n * ks + k] = (n < g.N && k < g.K) ? __bfloat162float(B[(size_t)k * g.ldb + n]) : 0.0f;
+  }
+  __syncthreads();
+  const bf16* A = static_cast<const bf16*>(g.A);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int m0 = (blockIdx.x * warps + warp) * R; m0 < g.M; m0 += gridDim.x * warps * R) {
+    float acc[R][NP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int n = 0; n < NP; ++n) acc[r][n] = 0.0f;
+    for (int k = 2 * lane; k < k2; k += 64) {
+      float a[R][2];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int m = m0 + r;
+        const bf16* ap = A + (size_t)m * g.lda + k;
+        if (vec2 && m < g.M && k + 1 < g.K) {
+          const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ap));
+          a[r][0] = t.x;
+          a[r][1] = t.y;
+        } else {
+          a[r][0] = (m < g.M && k < g.K) ? __bfloat162float(ap[0]) : 0.0f;
+          a[r][1] = (m < g.M && k + 1 < g.K) ? __bfloat162float(ap[1]) : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NP; ++n) {
+        const float2 b = *reinterpret_cast<const float2*>(&sbt[n * ks + k]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r][n] = fmaf(a[r][1], b.y, fmaf(a[r][0], b.x, acc[r][n]));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int n = 0; n < NP; ++n) {
+        const float v = warp_sum(acc[r][n]);
+        if (lane == n && n < g.N && m0 + r < g.M) epilogue_elem<TO, bf16>(g, g.bias, m0 + r, n, v);
+      }
+  }
+}
+
+// Input gradient, K <= 32: out[m][n] = sum_k A[m][k] B[n][k] (A K-major, B
+// K-major).  B is held in shared memory as [K][n8] (n8 = N rounded up to 8);
+// a thread computes eight consecutive outputs of a row.
+template <typename TO>
+__global__ void __launch_bounds__(256) skinny_dx_kernel(const GemmArgs g, int n8, int vec) {
+  extern __shared__ __align__(16) float sw[];
+  const bf16* B = static_cast<const bf16*>(g.B);
+  for (int i = threadIdx.x; i < n8 * g.K; i += blockDim.x) {
+    const int n = i / g.K, k = i - n * g.K;
+    sw[k * n8 + n] = n < g.N ? __bfloat162float(B[(size_t)n * g.ldb + k]) : 0.0f;
+  }
+  __syncthreads();
+  const bf16* A = static_cast<const bf16*>(g.A);
+  const int nc = n8 / 8;
+  const long long total = (long long)g.M * nc;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / nc), n0 = 8 * (int)(idx - (long long)m * nc);
+    const bf16* ap = A + (size_t)m * g.lda;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int k = 0; k < g.K; ++k) {
+      const float a = __bfloat162float(ap[k]);
+      const float4 w0 = *reinterpret_cast<const float4*>(&sw[k * n8 + n0]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&sw[k * n8 + n0 + 4]);
+      acc[0] = fmaf(a, w0.x, acc[0]); acc[1] = fmaf(a, w0.y, acc[1]);
+      acc[2] = fmaf(a, w0.z, acc[2]); acc[3] = fmaf(a, w0.w, acc[3]);
+      acc[4] = fmaf(a, w1.x, acc[4]); acc[5] = fmaf(a, w1.y, acc[5]);
+      acc[6] = fmaf(a, w1.z, acc[6]); acc[7] = fmaf(a, w1.w, acc[7]);
+    }
+    if (vec && n0 + 8 <= g.N) {
+      epilogue8_bf16(g, m, n0, acc);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (n0 + j < g.N) epilogue_elem<TO, bf16>(g, g.bias, m, n0 + j, acc[j]);
+    }
+  }
+}
+
+// Weight gradient, N <= NP, plain fp32 output: out[m][n] = sum_k A[k][m]
+// B[k][n] (A M-major, B N-major).  A block owns 32*MV rows of the output (MV
+// consecutive per lane) and a range of K; its eight warps take interleaved
+// k of that range with 64-row chunks of B staged in shared memory, then add
+// their partial sums in warp order (deterministic).  With several K ranges
+// (gridDim.y > 1) the blocks add into a zeroed output with atomics.
+template <int NP, int MV>
+__global__ void __launch_bounds__(256) skinny_dw_kernel(const GemmArgs g, int kper, int vec) {
+  __shared__ __align__(16) float sb[64][NP];
+  __shared__ float red[NP][MV][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mb = blockIdx.x * 32 * MV, m0 = mb + lane * MV;
+  const int k0 = blockIdx.y * kper, k1 = min(g.K, k0 + kper);
+  const bf16* A = static_cast<const bf16*>(g.A);
+  const bf16* B = static_cast<const bf16*>(g.B);
+  float acc[MV][NP];
+#pragma unroll
+  for (int j = 0; j < MV; ++j)
+#pragma unroll
+    for (int n = 0; n < NP; ++n) acc[j][n] = 0.0f;
+  for (int kc = k0; kc < k1; kc += 64) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * NP; i += blockDim.x) {
+      const int kk = i / NP, n = i - kk * NP, k = kc + kk;
+      sb[kk][n] = (k < k1 && n < g.N) ? __bfloat162float(B[(size_t)k * g.ldb + n]) : 0.0f;
+    }
+    __syncthreads();
+    const int kend = min(64, k1 - kc);
+#pragma unroll 4
+    for (int kk = warp; kk < kend; kk += 8) {
+      const bf16* ap = A + (size_t)(kc + kk) * g.lda + m0;
+      float a[MV];
+      if (vec && m0 + MV <= g.M) {
+        if constexpr (MV == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(ap);
+          const float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+          const float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+          a[0] = t0.x; a[1] = t0.y; a[2] = t1.x; a[3] = t1.y;
+        } else {
+          static_assert(MV == 2, "two or four rows per lane");
+          const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ap));
+          a[0] = t.x; a[1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < MV; ++j) a[j] = m0 + j < g.M ? __bfloat162float(ap[j]) : 0.0f;
+      }
+#pragma unroll
+      for (int n = 0; n < NP; n += 4) {
+        const float4 b = *reinterpret_cast<const float4*>(&sb[kk][n]);
+#pragma unroll
+        for (int j = 0; j < MV; ++j) {
+          acc[j][n] = fmaf(a[j], b.x, acc[j][n]);
+          acc[j][n + 1] = fmaf(a[j], b.y, acc[j][n + 1]);
+          acc[j][n + 2] = fmaf(a[j], b.z, acc[j][n + 2]);
+          acc[j][n + 3] = fmaf(a[j], b.w, acc[j][n + 3]);
+        }
+      }
+    }
+  }
+  for (int w = 0; w < 8; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int j = 0; j < MV; ++j)
+#pragma unroll
+        for (int n = 0; n < NP; ++n) red[n][j][lane] = (w ? red[n][j][lane] : 0.0f) + acc[j][n];
+    }
+    __syncthreads();
+  }
+  float* out = static_cast<float*>(g.out);
+  for (int i = threadIdx.x; i < NP * MV * 32; i += blockDim.x) {
+    const int n = i / (MV * 32), j = (i / 32) % MV, l = i % 32;
+    const int m = mb + l * MV + j;
+    if (m < g.M && n < g.N) {
+      float* o = out + (size_t)m * g.ldo + n;
+      if (gridDim.y > 1)
+        atomicAdd(o, red[n][j][l]);
+      else
+        *o = red[n][j][l];
+    }
+  }
+}
+
+constexpr size_t kSkinnySmem = 96 * 1024;
+
+template <int NP, int R, typename TO>
+cudaError_t launch_skinny_fwd(const GemmArgs& g, cudaStream_t s) {
+  const int k2 = (g.K + 63) & ~63;
+  const size_t smem = (size_t)NP * (k2 + 2) * 4;
+  auto kern = skinny_fwd_kernel<NP, R, TO>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkinnySmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int vec2 = (reinterpret_cast<uintptr_t>(g.A) & 3u) == 0 && (g.lda & 1) == 0;
+  const int need = (g.M + 8 * R - 1) / (8 * R);
+  const int grid = need < 2 * sm_count_simt() ? need : 2 * sm_count_simt();
+  kern<<<grid, 256, smem, s>>>(g, k2, vec2);
+  return cudaGetLastError();
+}
+
+template <typename TO>
+cudaError_t launch_skinny_dx(const GemmArgs& g, cudaStream_t s) {
+  const int n8 = (g.N + 7) & ~7;
+  const size_t smem = (size_t)n8 * g.K * 4;
+  auto kern = skinny_dx_kernel<TO>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkinnySmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const int vec = sizeof(TO) == 2 && g.aux_type == DT_BF16 && al(g.out) && al(g.out_z) &&
+                  al(g.saved) && al(g.resid) && ((g.ldo | g.ldz | g.lds | g.ldr) & 7) == 0;
+  const long long items = (long long)g.M * (n8 / 8);
+  const long long need = (items + 255) / 256;
+  const int grid = (int)(need < 2LL * sm_count_simt() ? need : 2LL * sm_count_simt());
+  kern<<<grid, 256, smem, s>>>(g, n8, vec);
+  return cudaGetLastError();
+}
+
+template <int NP, int MV>
+cudaError_t launch_skinny_dw(const GemmArgs& g, cudaStream_t s) {
+  const int bx = (g.M + 32 * MV - 1) / (32 * MV);
+  int ks = (sm_count_simt() + bx - 1) / bx;       // about one block per SM
+  const int kmax = (g.K + 63) / 64;               // at least 64 rows of K per block
+  if (ks > kmax) ks = kmax;
+  if (ks < 1) ks = 1;
+  const int kper = (g.K + ks - 1) / ks;
+  ks = (g.K + kper - 1) / kper;
+  if (ks > 1) {
+    cudaError_t e = g.ldo == g.N
+                        ? cudaMemsetAsync(g.out, 0, (size_t)g.M * g.N * 4, s)
+                        : cudaMemset2DAsync(g.out, (size_t)g.ldo * 4, 0, (size_t)g.N * 4, g.M, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int vec = (reinterpret_cast<uintptr_t>(g.A) & (2u * MV - 1)) == 0 && (g.lda % MV) == 0;
+  skinny_dw_kernel<NP, MV><<<dim3(bx, ks), 256, 0, s>>>(g, kper, vec);
+  return cudaGetLastError();
+}
+
+// Which narrow-side kernel runs g (0 forward, 1 input gradient, 2 weight
+// gradient); false if none does.
+bool skinny_kind(const GemmArgs& g, int* kind) {
+  if (g.in_type != DT_BF16 || g.K <= 0) return false;
+  const bool plain = !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  if (!g.a_mn && !g.b_k && g.N <= 32 && (size_t)((g.N <= 16 ? 16 : 32) * (((g.K + 63) & ~63) + 2)) * 4 <= kSkinnySmem &&
+      (g.aux_type == DT_BF16 || (!g.out_z && !g.dact && !g.resid))) {
+    *kind = 0;   // forward
+    return true;
+  }
+  if (!g.a_mn && g.b_k && g.K <= 32 && (size_t)((g.N + 7) & ~7) * g.K * 4 <= kSkinnySmem &&
+      (g.aux_type == DT_BF16 || (!g.out_z && !g.dact && !g.resid))) {
+    *kind = 1;   // input gradient
+    return true;
+  }
+  if (g.a_mn && !g.b_k && g.N <= 32 && g.out_type == DT_F32 && plain) {
+    *kind = 2;   // weight gradient
+    return true;
+  }
+  return false;
+}
+
+cudaError_t gemm_skinny(const GemmArgs& g, int kind, cudaStream_t s) {
+  const bool f32 = g.out_type == DT_F32;
+  if (kind == 0) {
+    if (g.N <= 16) return f32 ? launch_skinny_fwd<16, 4, float>(g, s) : launch_skinny_fwd<16, 4, bf16>(g, s);
+    return f32 ? launch_skinny_fwd<32, 2, float>(g, s) : launch_skinny_fwd<32, 2, bf16>(g, s);
+  }
+  if (kind == 1) return f32 ? launch_skinny_dx<float>(g, s) : launch_skinny_dx<bf16>(g, s);
+  if (g.N <= 16) return launch_skinny_dw<16, 4>(g, s);
+  return launch_skinny_dw<32, 2>(g, s);
+}
+
 template <typename T, typename TO, typename TX, bool A_MN, bool B_K, bool COMP = false>
 cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
@@ -308,10 +643,17 @@ cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
 
 }  // namespace
 
+bool gemm_simt_skinny(const GemmArgs& g) {
+  int kind = 0;
+  return skinny_kind(g, &kind);
+}
+
 // Layouts used by the schedule: forward (A K-major, B N-major), dX (A K-major,
 // B K-major), dW (A M-major, B N-major, fp32 output).
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  int kind = 0;
+  if (skinny_kind(g, &kind)) return gemm_skinny(g, kind, s);
   if (g.a_mn && !g.b_k && g.N <= 32 && g.out_type == DT_F32 && !g.act && !g.dact && !g.resid &&
       !g.out_z) {   // narrow weight gradient
     if (g.in_type == DT_F32) return launch_dw_narrow<float, float, float>(g, s);

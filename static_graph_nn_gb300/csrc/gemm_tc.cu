@@ -410,19 +410,9 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
     attr_set = true;
   }
   const int tiles = P.tiles_m * P.tiles_n;
-  // Split-K for plain fp32 outputs (weight gradients) when the tiles leave
-  // SMs idle: the split count that minimises rounds of work / splits, with at
-  // least 4 K blocks per split; the partial sums are added into a zeroed output.
-  const bool plain = sizeof(TO) == 4 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
-  if (plain && tiles < num_sms()) {
-    double best = 1.0;
-    for (int sp = 2; sp <= 8 && P.k_blocks / sp >= 4; ++sp) {
-      const double cost = (double)((tiles * sp + num_sms() - 1) / num_sms()) / sp + 0.02 * sp;
-      if (cost < best - 1e-9) {
-        best = cost;
-        P.splits = sp;
-      }
-    }
+  {
+    double steps;
+    P.splits = gemm_tc_splits(g, &steps);
     if (P.splits > 1) {
       P.kb_per = (P.k_blocks + P.splits - 1) / P.splits;
       P.splits = (P.k_blocks + P.kb_per - 1) / P.kb_per;
@@ -449,6 +439,34 @@ bool gemm_tc_eligible(const GemmArgs& g) {
   if (g.a_mn && g.b_k) return false;
   if (g.out_type == DT_F32 && !g.a_mn) return false;   // only dW writes fp32
   return encode_fn() != nullptr;
+}
+
+// Split-K for plain fp32 outputs (weight gradients) when the 128x256 tiles
+// leave SMs idle: the split count that minimises rounds of work / splits, with
+// at least 4 K blocks per split; the partial sums are added into a zeroed
+// output.  *steps: the estimated duration in K-block steps of one SM at the
+// SM-pair kernel's per-SM MMA rate; this kernel's steps take about 1.5x as
+// long (one SM's shared memory feeds its 128x256 MMAs at about 2/3 of their
+// rate).
+int gemm_tc_splits(const GemmArgs& g, double* steps) {
+  const int sms = num_sms();
+  const int tiles = ((g.M + TC_BM - 1) / TC_BM) * ((g.N + 255) / 256);
+  const int kb = (g.K + TC_BK - 1) / TC_BK;
+  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  int splits = 1;
+  double best = (double)((tiles + sms - 1) / sms);
+  if (plain && tiles < sms) {
+    best = 1.0;
+    for (int sp = 2; sp <= 8 && kb / sp >= 4; ++sp) {
+      const double cost = (double)((tiles * sp + sms - 1) / sms) / sp + 0.02 * sp;
+      if (cost < best - 1e-9) {
+        best = cost;
+        splits = sp;
+      }
+    }
+  }
+  if (steps) *steps = 1.5 * best * kb;
+  return splits;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, int* err, cudaStream_t s) {

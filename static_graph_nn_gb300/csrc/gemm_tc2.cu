@@ -44,6 +44,7 @@ constexpr uint32_t P_B_BYTES = P_BNH * P_BK * 2;
 struct PairParams {
   GemmArgs g;
   int tiles_m, tiles_n, k_blocks;   // tiles_m counts 256-row pair tiles
+  int splits, kb_per;               // split-K: K blocks [s*kb_per, (s+1)*kb_per) per split
   int vec;
   int* err;
 };
@@ -125,6 +126,23 @@ __device__ __forceinline__ void st8f(bf16* p, const float* f) {
     w[i] = *reinterpret_cast<uint32_t*>(&h);
   }
   *reinterpret_cast<uint4*>(p) = u;
+}
+
+// One split's partial sums of 32 columns of one row, added into the (zeroed)
+// fp32 output; plain weight-gradient outputs only.
+__device__ __forceinline__ void split_add32(const GemmArgs& g, bool vec, int m, int n0,
+                                            const float (&v)[32]) {
+  float* out = static_cast<float*>(g.out) + (size_t)m * g.ldo + n0;
+  if (vec && n0 + 32 <= g.N) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      atomicAdd(reinterpret_cast<float4*>(out) + q,
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (n0 + j < g.N) atomicAdd(out + j, v[j]);
 }
 
 // Epilogue of 32 columns of one row; identical arithmetic to gemm_tc.cu.
@@ -223,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const bool leader = rank == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int n_tiles = P.tiles_m * P.tiles_n;
+  const int n_items = P.tiles_m * P.tiles_n * P.splits;   // (tile, K split) work items
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
@@ -253,10 +271,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = pair; tile < n_tiles && !*abort_flag; tile += npairs) {
+      for (int item = pair; item < n_items && !*abort_flag; item += npairs) {
+        const int tile = item / P.splits, sp = item % P.splits;
         const int m0 = (tile / P.tiles_n) * 2 * P_BM + rank * P_BM;
         const int n0 = (tile % P.tiles_n) * P_BN + rank * P_BNH;
-        for (int kb = 0; kb < P.k_blocks; ++kb) {
+        const int kb0 = sp * P.kb_per, kb1 = min(P.k_blocks, kb0 + P.kb_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
           // both CTAs' bytes complete on the leader's full barrier
           if (leader) mbar_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
@@ -287,14 +307,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int tile = pair; tile < n_tiles && !*abort_flag; tile += npairs, ++it) {
+      for (int item = pair; item < n_items && !*abort_flag; item += npairs, ++it) {
+        const int sp = item % P.splits;
+        const int kb0 = sp * P.kb_per, kb1 = min(P.k_blocks, kb0 + P.kb_per);
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_cluster(&tempty[acc], use ^ 1)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * P_BN);
         bool ok = true;
-        for (int kb = 0; kb < P.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a = smem_u32(sA + stage * P_A_BYTES);
@@ -305,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                                      : smem_desc(a + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(b + k * 2048, 64 * P_BK * 2, 1024)
                                      : smem_desc(b + k * 32, 16, 1024);
-            mma_bf16_pair(d, ad, bd, idesc, (kb | k) ? 1u : 0u);
+            mma_bf16_pair(d, ad, bd, idesc, (kb > kb0 || k) ? 1u : 0u);
           }
           mma_commit_pair(&empty[stage]);        // frees stage s in both CTAs
           if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
@@ -321,7 +343,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t leader_tempty[2] = {map_to(&tempty[0], 0), map_to(&tempty[1], 0)};
     int it = 0;
-    for (int tile = pair; tile < n_tiles; tile += npairs, ++it) {
+    for (int item = pair; item < n_items; item += npairs, ++it) {
+      const int tile = item / P.splits;
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], use)) { *abort_flag = 1; atomicExch(P.err, 1); break; }
@@ -337,8 +360,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         float v[32];
         tmem_ld32(taddr + c * 32, v);
         if (m < P.g.M && n0 + c * 32 < P.g.N) {
-          if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
-          epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+          if (P.splits > 1) {
+            split_add32(P.g, P.vec != 0, m, n0 + c * 32, v);
+          } else {
+            if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
+            epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+          }
         }
       }
       if (P.g.lse_part && m < P.g.M && n0 + half * (P_BN / 2) < P.g.N)
@@ -402,6 +429,63 @@ int sm_count2() {
   return n;
 }
 
+constexpr size_t kPairSmem = 1024 + (size_t)P_STAGES * (P_A_BYTES + P_B_BYTES) + (2 * P_STAGES + 4) * 8 + 16;
+
+// Clusters of two that can be resident at once (GPCs may not pair every SM);
+// every instantiation of the kernel has the same shape of launch.
+int pair_slots() {
+  static int n = 0;
+  if (!n) {
+    auto kern = gemm_pair_kernel<float, true, true>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sm_count2() / 2));
+    cfg.blockDim = dim3(P_THREADS);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess || c <= 0) {
+      cudaGetLastError();
+      c = sm_count2() / 2;
+    }
+    n = c;
+  }
+  return n;
+}
+
+// Split-K of the pair kernel, chosen as for the single-SM kernel (plain fp32
+// outputs whose 256x256 tiles leave pairs idle, at least 4 K blocks per
+// split), with a larger charge per split: a pair's partial tile is twice a
+// single SM's, so each split adds twice the atomic traffic per slot.  *steps:
+// estimated duration in K-block steps of one SM.
+int pair_splits(const GemmArgs& g, double* steps) {
+  const int slots = pair_slots();
+  const int tiles = ((g.M + 2 * P_BM - 1) / (2 * P_BM)) * ((g.N + P_BN - 1) / P_BN);
+  const int kb = (g.K + P_BK - 1) / P_BK;
+  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  int splits = 1;
+  double best = (double)((tiles + slots - 1) / slots);
+  if (plain && tiles < slots) {
+    best = 1.0;
+    for (int sp = 2; sp <= 8 && kb / sp >= 4; ++sp) {
+      const double cost = (double)((tiles * sp + slots - 1) / slots) / sp + 0.05 * sp;
+      if (cost < best - 1e-9) {
+        best = cost;
+        splits = sp;
+      }
+    }
+  }
+  if (steps) *steps = best * kb;
+  return splits;
+}
+
 template <typename TO, bool A_MN, bool B_MN>
 cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
   CUtensorMap ma, mb;
@@ -415,13 +499,19 @@ cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
   P.tiles_m = (g.M + 2 * P_BM - 1) / (2 * P_BM);
   P.tiles_n = (g.N + P_BN - 1) / P_BN;
   P.k_blocks = (g.K + P_BK - 1) / P_BK;
+  P.splits = pair_splits(g, nullptr);
+  P.kb_per = P.k_blocks;
+  if (P.splits > 1) {
+    P.kb_per = (P.k_blocks + P.splits - 1) / P.splits;
+    P.splits = (P.k_blocks + P.kb_per - 1) / P.kb_per;
+  }
   P.err = err;
   {
     auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
     P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) && (lds & 7) == 0;
   }
-  const size_t smem = 1024 + (size_t)P_STAGES * (P_A_BYTES + P_B_BYTES) + (2 * P_STAGES + 4) * 8 + 16;
+  const size_t smem = kPairSmem;
   auto kern = gemm_pair_kernel<TO, A_MN, B_MN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -429,29 +519,15 @@ cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  static int max_pairs = 0;
-  if (!max_pairs) {   // clusters of two that fit at once (GPCs may not pair every SM)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sm_count2() / 2));
-    cfg.blockDim = dim3(P_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = 2;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = sm_count2() / 2;
-    }
-    max_pairs = n;
+  if (P.splits > 1) {   // the splits' partial sums are added into a zeroed output
+    cudaError_t e = g.ldo == g.N
+                        ? cudaMemsetAsync(g.out, 0, (size_t)g.M * g.N * 4, s)
+                        : cudaMemset2DAsync(g.out, (size_t)g.ldo * 4, 0, (size_t)g.N * 4, g.M, s);
+    if (e != cudaSuccess) return e;
   }
-  const int tiles = P.tiles_m * P.tiles_n;
-  int pairs = max_pairs;
-  if (tiles < pairs) pairs = tiles;
+  const int items = P.tiles_m * P.tiles_n * P.splits;
+  int pairs = pair_slots();
+  if (items < pairs) pairs = items;
   kern<<<2 * pairs, P_THREADS, smem, s>>>(ma, mb, P);
   return cudaGetLastError();
 }
@@ -459,8 +535,13 @@ cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
 }  // namespace
 
 bool gemm_pair_eligible(const GemmArgs& g) {
-  // worth a pair: at least one full 256x256 tile of work per pair on average
-  return g.M >= 256 && g.N >= 256 && g.K >= 64 && (long long)g.M * g.N >= 256LL * 256 * 64;
+  // the estimated durations of the two kernels, waves of (split) tiles times
+  // their K-block steps; below 128 rows or columns a pair is mostly padding
+  if (g.M < 128 || g.N < 128 || g.K < 64) return false;
+  double pair_steps = 0, single_steps = 0;
+  pair_splits(g, &pair_steps);
+  gemm_tc_splits(g, &single_steps);
+  return pair_steps < single_steps;
 }
 
 cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s) {

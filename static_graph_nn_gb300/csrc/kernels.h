@@ -38,12 +38,19 @@ struct GemmArgs {
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
+// Whether gemm_simt runs g on its narrow-side bf16 kernels (N <= 32 forward
+// or weight gradient, K <= 32 input gradient).
+bool gemm_simt_skinny(const GemmArgs& g);
 // tcgen05/TMA version for bf16 operands whose rows are 16-byte aligned.
 // *err is set to 1 if a bounded pipeline wait expires.
 bool gemm_tc_eligible(const GemmArgs& g);
 cudaError_t gemm_tc(const GemmArgs& g, int* err, cudaStream_t s);
-// Same on a pair of SMs (tcgen05 cta_group::2, 256x256 tiles); requires
-// gemm_tc_eligible(g) as well.
+// Split count of the single-SM tensor-core GEMM for g and, in *steps (may be
+// NULL), its estimated duration in K-block steps of one SM.
+int gemm_tc_splits(const GemmArgs& g, double* steps);
+// Same on a pair of SMs (tcgen05 cta_group::2, 256x256 tiles), used where it
+// is estimated faster than the single-SM kernel; requires gemm_tc_eligible(g)
+// as well.
 bool gemm_pair_eligible(const GemmArgs& g);
 cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s);
 

@@ -275,6 +275,7 @@ std::string gemm_name(const mg_plan* p, const char* what, int layer, const GemmA
   const char* kind = g.in_type != DT_BF16 ? "f32-ffma"
                      : pair_path(p, g)    ? "bf16-tcgen05x2"
                      : tc_path(p, g)      ? "bf16-tcgen05"
+                     : gemm_simt_skinny(g) ? "bf16-skinny"
                                           : "bf16-simt";
   snprintf(b, sizeof b, "%s[l%d] %dx%dx%d %s", what, layer, g.M, g.N, g.K, kind);
   return b;
