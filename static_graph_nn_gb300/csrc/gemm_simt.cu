@@ -360,20 +360,77 @@ __device__ __forceinline__ void epilogue8_bf16(const GemmArgs& g, int m, int n0,
   pack8(static_cast<bf16*>(g.out) + (size_t)m * g.ldo + n0, v);
 }
 
+// Copies the bf16 matrix src (rows x cols, row stride ld) into shared memory
+// through put(r, c, value) with many loads in flight: 16-byte loads of the
+// flat array when the rows are contiguous and aligned, else eight scalar
+// loads per thread per round.
+template <typename F>
+__device__ __forceinline__ void stage_bf16(const bf16* src, int rows, int cols, long long ld,
+                                           F put) {
+  const int total = rows * cols;
+  if (ld == cols && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    const int nv = total / 8;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int base = threadIdx.x; base < nv; base += 4 * blockDim.x) {
+      uint4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = base + u * blockDim.x;
+        t[u] = q < nv ? s4[q] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = base + u * blockDim.x;
+        if (q >= nv) continue;
+        const uint32_t w[4] = {t[u].x, t[u].y, t[u].z, t[u].w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[p]));
+          const int e = 8 * q + 2 * p;
+          const int r0 = e / cols, r1 = (e + 1) / cols;
+          put(r0, e - r0 * cols, f.x);
+          put(r1, e + 1 - r1 * cols, f.y);
+        }
+      }
+    }
+    for (int e = 8 * nv + threadIdx.x; e < total; e += blockDim.x) {
+      const int r = e / cols;
+      put(r, e - r * cols, __bfloat162float(src[e]));
+    }
+    return;
+  }
+  for (int base = threadIdx.x; base < total; base += 8 * blockDim.x) {
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * blockDim.x;
+      const int r = i / cols, c = i - r * cols;
+      t[u] = i < total ? __bfloat162float(src[(size_t)r * ld + c]) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * blockDim.x;
+      if (i < total) {
+        const int r = i / cols;
+        put(r, i - r * cols, t[u]);
+      }
+    }
+  }
+}
+
 // Forward, N <= NP: out[m][n] = sum_k A[m][k] B[k][n] (A K-major, B N-major).
 // B is held transposed in shared memory ([NP][ks], zero padded to k2, a
-// multiple of 64).  A warp owns R rows at a time; lane l takes the bf16 pairs
-// at k = 2l + 64i of each row; the partial sums are reduced across the warp
-// and lane n applies the epilogue to column n.
+// multiple of 256).  A warp owns R rows at a time; lane l takes the eight
+// consecutive k at 8l + 256i of each row (one 16-byte load); the partial sums
+// are reduced across the warp and lane n applies the epilogue to column n.
 template <int NP, int R, typename TO>
-__global__ void __launch_bounds__(256) skinny_fwd_kernel(const GemmArgs g, int k2, int vec2) {
+__global__ void __launch_bounds__(256) skinny_fwd_kernel(const GemmArgs g, int k2, int vec8) {
   extern __shared__ __align__(16) float sbt[];
-  const int ks = k2 + 2;   // row stride: float2-aligned, rows two banks apart
-  const bf16* B = static_cast<const bf16*>(g.B);
-  for (int i = threadIdx.x; i < k2 * NP; i += blockDim.x) {
-    const int k = i / NP, n = i - k * NP;
-    sbt[n * ks + k] = (n < g.N && k < g.K) ? __bfloat162float(B[(size_t)k * g.ldb + n]) : 0.0f;
-  }
+  const int ks = k2 + 4;   // row stride: 16-byte aligned, rows four banks apart
+  for (int i = threadIdx.x; i < NP * ks; i += blockDim.x) sbt[i] = 0.0f;
+  __syncthreads();
+  stage_bf16(static_cast<const bf16*>(g.B), g.K, g.N, g.ldb,
+             [&](int k, int n, float v) { sbt[n * ks + k] = v; });
   __syncthreads();
   const bf16* A = static_cast<const bf16*>(g.A);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,26 +441,32 @@ __global__ void __launch_bounds__(256) skinny_fwd_kernel(const GemmArgs g, int k
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int n = 0; n < NP; ++n) acc[r][n] = 0.0f;
-    for (int k = 2 * lane; k < k2; k += 64) {
-      float a[R][2];
+    for (int k = 8 * lane; k < k2; k += 256) {
+      float a[R][8];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int m = m0 + r;
         const bf16* ap = A + (size_t)m * g.lda + k;
-        if (vec2 && m < g.M && k + 1 < g.K) {
-          const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ap));
-          a[r][0] = t.x;
-          a[r][1] = t.y;
+        if (vec8 && m < g.M && k + 8 <= g.K) {
+          unpack8(ap, a[r]);
         } else {
-          a[r][0] = (m < g.M && k < g.K) ? __bfloat162float(ap[0]) : 0.0f;
-          a[r][1] = (m < g.M && k + 1 < g.K) ? __bfloat162float(ap[1]) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[r][j] = (m < g.M && k + j < g.K) ? __bfloat162float(ap[j]) : 0.0f;
         }
       }
 #pragma unroll
       for (int n = 0; n < NP; ++n) {
-        const float2 b = *reinterpret_cast<const float2*>(&sbt[n * ks + k]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&sbt[n * ks + k]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&sbt[n * ks + k + 4]);
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[r][n] = fmaf(a[r][1], b.y, fmaf(a[r][0], b.x, acc[r][n]));
+        for (int r = 0; r < R; ++r) {
+          float t = acc[r][n];
+          t = fmaf(a[r][0], b0.x, t); t = fmaf(a[r][1], b0.y, t);
+          t = fmaf(a[r][2], b0.z, t); t = fmaf(a[r][3], b0.w, t);
+          t = fmaf(a[r][4], b1.x, t); t = fmaf(a[r][5], b1.y, t);
+          t = fmaf(a[r][6], b1.z, t); t = fmaf(a[r][7], b1.w, t);
+          acc[r][n] = t;
+        }
       }
     }
 #pragma unroll
@@ -422,11 +485,10 @@ __global__ void __launch_bounds__(256) skinny_fwd_kernel(const GemmArgs g, int k
 template <typename TO>
 __global__ void __launch_bounds__(256) skinny_dx_kernel(const GemmArgs g, int n8, int vec) {
   extern __shared__ __align__(16) float sw[];
-  const bf16* B = static_cast<const bf16*>(g.B);
-  for (int i = threadIdx.x; i < n8 * g.K; i += blockDim.x) {
-    const int n = i / g.K, k = i - n * g.K;
-    sw[k * n8 + n] = n < g.N ? __bfloat162float(B[(size_t)n * g.ldb + k]) : 0.0f;
-  }
+  for (int i = threadIdx.x; i < n8 * g.K; i += blockDim.x) sw[i] = 0.0f;
+  __syncthreads();
+  stage_bf16(static_cast<const bf16*>(g.B), g.N, g.K, g.ldb,
+             [&](int n, int k, float v) { sw[k * n8 + n] = v; });
   __syncthreads();
   const bf16* A = static_cast<const bf16*>(g.A);
   const int nc = n8 / 8;
@@ -459,60 +521,66 @@ __global__ void __launch_bounds__(256) skinny_dx_kernel(const GemmArgs g, int n8
 
 // Weight gradient, N <= NP, plain fp32 output: out[m][n] = sum_k A[k][m]
 // B[k][n] (A M-major, B N-major).  A block owns 32*MV rows of the output (MV
-// consecutive per lane) and a range of K; its eight warps take interleaved
-// k of that range with 64-row chunks of B staged in shared memory, then add
-// their partial sums in warp order (deterministic).  With several K ranges
-// (gridDim.y > 1) the blocks add into a zeroed output with atomics.
+// consecutive per lane) and kper rows of K, whose rows of B it holds in shared
+// memory; its eight warps take interleaved k, U rows' loads in flight at a
+// time, then add their partial sums in warp order (deterministic).  With
+// several K ranges (gridDim.y > 1) the blocks add into a zeroed output with
+// atomics.
 template <int NP, int MV>
 __global__ void __launch_bounds__(256) skinny_dw_kernel(const GemmArgs g, int kper, int vec) {
-  __shared__ __align__(16) float sb[64][NP];
+  constexpr int U = 8;
+  extern __shared__ __align__(16) float sb[];   // [kper][NP]
   __shared__ float red[NP][MV][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mb = blockIdx.x * 32 * MV, m0 = mb + lane * MV;
-  const int k0 = blockIdx.y * kper, k1 = min(g.K, k0 + kper);
+  const int k0 = blockIdx.y * kper, kn = min(g.K, k0 + kper) - k0;
   const bf16* A = static_cast<const bf16*>(g.A);
-  const bf16* B = static_cast<const bf16*>(g.B);
+  for (int i = threadIdx.x; i < kn * NP; i += blockDim.x) sb[i] = 0.0f;
+  __syncthreads();
+  stage_bf16(static_cast<const bf16*>(g.B) + (size_t)k0 * g.ldb, kn, g.N, g.ldb,
+             [&](int r, int n, float v) { sb[r * NP + n] = v; });
+  __syncthreads();
   float acc[MV][NP];
 #pragma unroll
   for (int j = 0; j < MV; ++j)
 #pragma unroll
     for (int n = 0; n < NP; ++n) acc[j][n] = 0.0f;
-  for (int kc = k0; kc < k1; kc += 64) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < 64 * NP; i += blockDim.x) {
-      const int kk = i / NP, n = i - kk * NP, k = kc + kk;
-      sb[kk][n] = (k < k1 && n < g.N) ? __bfloat162float(B[(size_t)k * g.ldb + n]) : 0.0f;
-    }
-    __syncthreads();
-    const int kend = min(64, k1 - kc);
-#pragma unroll 4
-    for (int kk = warp; kk < kend; kk += 8) {
-      const bf16* ap = A + (size_t)(kc + kk) * g.lda + m0;
-      float a[MV];
-      if (vec && m0 + MV <= g.M) {
+  for (int kk = warp; kk < kn; kk += 8 * U) {
+    float a[U][MV];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = kk + 8 * u;
+      const bf16* ap = A + (size_t)(k0 + r) * g.lda + m0;
+      if (r < kn && vec && m0 + MV <= g.M) {
         if constexpr (MV == 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(ap);
-          const float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-          const float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-          a[0] = t0.x; a[1] = t0.y; a[2] = t1.x; a[3] = t1.y;
+          const uint2 q = *reinterpret_cast<const uint2*>(ap);
+          const float2 t0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+          const float2 t1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+          a[u][0] = t0.x; a[u][1] = t0.y; a[u][2] = t1.x; a[u][3] = t1.y;
         } else {
           static_assert(MV == 2, "two or four rows per lane");
           const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(ap));
-          a[0] = t.x; a[1] = t.y;
+          a[u][0] = t.x; a[u][1] = t.y;
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < MV; ++j) a[j] = m0 + j < g.M ? __bfloat162float(ap[j]) : 0.0f;
+        for (int j = 0; j < MV; ++j)
+          a[u][j] = (r < kn && m0 + j < g.M) ? __bfloat162float(ap[j]) : 0.0f;
       }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = kk + 8 * u;
+      if (r >= kn) break;
 #pragma unroll
       for (int n = 0; n < NP; n += 4) {
-        const float4 b = *reinterpret_cast<const float4*>(&sb[kk][n]);
+        const float4 b = *reinterpret_cast<const float4*>(&sb[r * NP + n]);
 #pragma unroll
         for (int j = 0; j < MV; ++j) {
-          acc[j][n] = fmaf(a[j], b.x, acc[j][n]);
-          acc[j][n + 1] = fmaf(a[j], b.y, acc[j][n + 1]);
-          acc[j][n + 2] = fmaf(a[j], b.z, acc[j][n + 2]);
-          acc[j][n + 3] = fmaf(a[j], b.w, acc[j][n + 3]);
+          acc[j][n] = fmaf(a[u][j], b.x, acc[j][n]);
+          acc[j][n + 1] = fmaf(a[u][j], b.y, acc[j][n + 1]);
+          acc[j][n + 2] = fmaf(a[u][j], b.z, acc[j][n + 2]);
+          acc[j][n + 3] = fmaf(a[u][j], b.w, acc[j][n + 3]);
         }
       }
     }
@@ -542,62 +610,73 @@ __global__ void __launch_bounds__(256) skinny_dw_kernel(const GemmArgs g, int kp
 
 constexpr size_t kSkinnySmem = 96 * 1024;
 
+size_t skinny_fwd_smem(const GemmArgs& g) {
+  const int np = g.N <= 16 ? 16 : 32;
+  return (size_t)np * (((g.K + 255) & ~255) + 4) * 4;
+}
+
+size_t skinny_dx_smem(const GemmArgs& g) { return (size_t)((g.N + 7) & ~7) * g.K * 4; }
+
+template <typename K>
+cudaError_t allow_smem(K kern, bool& done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkinnySmem);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
 template <int NP, int R, typename TO>
 cudaError_t launch_skinny_fwd(const GemmArgs& g, cudaStream_t s) {
-  const int k2 = (g.K + 63) & ~63;
-  const size_t smem = (size_t)NP * (k2 + 2) * 4;
-  auto kern = skinny_fwd_kernel<NP, R, TO>;
   static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkinnySmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int vec2 = (reinterpret_cast<uintptr_t>(g.A) & 3u) == 0 && (g.lda & 1) == 0;
+  cudaError_t e = allow_smem(skinny_fwd_kernel<NP, R, TO>, attr);
+  if (e != cudaSuccess) return e;
+  const int k2 = (g.K + 255) & ~255;
+  const int vec8 = (reinterpret_cast<uintptr_t>(g.A) & 15u) == 0 && (g.lda & 7) == 0;
   const int need = (g.M + 8 * R - 1) / (8 * R);
   const int grid = need < 2 * sm_count_simt() ? need : 2 * sm_count_simt();
-  kern<<<grid, 256, smem, s>>>(g, k2, vec2);
+  skinny_fwd_kernel<NP, R, TO><<<grid, 256, skinny_fwd_smem(g), s>>>(g, k2, vec8);
   return cudaGetLastError();
 }
 
 template <typename TO>
 cudaError_t launch_skinny_dx(const GemmArgs& g, cudaStream_t s) {
-  const int n8 = (g.N + 7) & ~7;
-  const size_t smem = (size_t)n8 * g.K * 4;
-  auto kern = skinny_dx_kernel<TO>;
   static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkinnySmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = allow_smem(skinny_dx_kernel<TO>, attr);
+  if (e != cudaSuccess) return e;
+  const int n8 = (g.N + 7) & ~7;
   auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const int vec = sizeof(TO) == 2 && g.aux_type == DT_BF16 && al(g.out) && al(g.out_z) &&
                   al(g.saved) && al(g.resid) && ((g.ldo | g.ldz | g.lds | g.ldr) & 7) == 0;
   const long long items = (long long)g.M * (n8 / 8);
   const long long need = (items + 255) / 256;
-  const int grid = (int)(need < 2LL * sm_count_simt() ? need : 2LL * sm_count_simt());
-  kern<<<grid, 256, smem, s>>>(g, n8, vec);
+  const int grid = (int)(need < 4LL * sm_count_simt() ? need : 4LL * sm_count_simt());
+  skinny_dx_kernel<TO><<<grid, 256, skinny_dx_smem(g), s>>>(g, n8, vec);
   return cudaGetLastError();
 }
 
 template <int NP, int MV>
 cudaError_t launch_skinny_dw(const GemmArgs& g, cudaStream_t s) {
+  static bool attr = false;
+  cudaError_t e = allow_smem(skinny_dw_kernel<NP, MV>, attr);
+  if (e != cudaSuccess) return e;
   const int bx = (g.M + 32 * MV - 1) / (32 * MV);
-  int ks = (sm_count_simt() + bx - 1) / bx;       // about one block per SM
-  const int kmax = (g.K + 63) / 64;               // at least 64 rows of K per block
+  const int kcap = (int)(kSkinnySmem / (NP * 4)) & ~7;   // rows of B a block can hold
+  int ks = (sm_count_simt() + bx - 1) / bx;              // about one block per SM
+  const int kmax = (g.K + 63) / 64;                      // at least 64 rows of K per block
   if (ks > kmax) ks = kmax;
+  if (ks < (g.K + kcap - 1) / kcap) ks = (g.K + kcap - 1) / kcap;
   if (ks < 1) ks = 1;
-  const int kper = (g.K + ks - 1) / ks;
+  int kper = (g.K + ks - 1) / ks;
+  kper = (kper + 7) & ~7;                                // 16-byte aligned row ranges of B
+  if (kper > kcap) kper = kcap;
   ks = (g.K + kper - 1) / kper;
   if (ks > 1) {
-    cudaError_t e = g.ldo == g.N
-                        ? cudaMemsetAsync(g.out, 0, (size_t)g.M * g.N * 4, s)
-                        : cudaMemset2DAsync(g.out, (size_t)g.ldo * 4, 0, (size_t)g.N * 4, g.M, s);
+    e = g.ldo == g.N ? cudaMemsetAsync(g.out, 0, (size_t)g.M * g.N * 4, s)
+                     : cudaMemset2DAsync(g.out, (size_t)g.ldo * 4, 0, (size_t)g.N * 4, g.M, s);
     if (e != cudaSuccess) return e;
   }
   const int vec = (reinterpret_cast<uintptr_t>(g.A) & (2u * MV - 1)) == 0 && (g.lda % MV) == 0;
-  skinny_dw_kernel<NP, MV><<<dim3(bx, ks), 256, 0, s>>>(g, kper, vec);
+  skinny_dw_kernel<NP, MV><<<dim3(bx, ks), 256, (size_t)kper * NP * 4, s>>>(g, kper, vec);
   return cudaGetLastError();
 }
 
@@ -606,12 +685,12 @@ cudaError_t launch_skinny_dw(const GemmArgs& g, cudaStream_t s) {
 bool skinny_kind(const GemmArgs& g, int* kind) {
   if (g.in_type != DT_BF16 || g.K <= 0) return false;
   const bool plain = !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
-  if (!g.a_mn && !g.b_k && g.N <= 32 && (size_t)((g.N <= 16 ? 16 : 32) * (((g.K + 63) & ~63) + 2)) * 4 <= kSkinnySmem &&
+  if (!g.a_mn && !g.b_k && g.N <= 32 && skinny_fwd_smem(g) <= kSkinnySmem &&
       (g.aux_type == DT_BF16 || (!g.out_z && !g.dact && !g.resid))) {
     *kind = 0;   // forward
     return true;
   }
-  if (!g.a_mn && g.b_k && g.K <= 32 && (size_t)((g.N + 7) & ~7) * g.K * 4 <= kSkinnySmem &&
+  if (!g.a_mn && g.b_k && g.K <= 32 && skinny_dx_smem(g) <= kSkinnySmem &&
       (g.aux_type == DT_BF16 || (!g.out_z && !g.dact && !g.resid))) {
     *kind = 1;   // input gradient
     return true;
