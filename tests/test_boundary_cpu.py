@@ -88,3 +88,68 @@ def test_null_arguments(lib):
     assert lib.mg_train_step(None, None, None, None, None, None, None, 0.1, 1, None) == binding.MG_ERR_INVALID_ARG
     assert lib.mg_forward(None, None, None, None, None) == binding.MG_ERR_INVALID_ARG
     assert lib.mg_last_error(None)
+
+
+def _create_raw(lib, layers, loss=0, precision=0, optimizer=1, beta1=0.9, beta2=0.999, eps=1e-8):
+    arr = (binding.mg_layer * max(1, len(layers)))(*[binding.layer_struct(l) for l in layers])
+    d = binding.mg_graph_desc()
+    d.batch, d.n_layers, d.layers = 8, len(layers), arr
+    d.loss, d.precision, d.optimizer = loss, precision, optimizer
+    d.beta1, d.beta2, d.adam_eps = beta1, beta2, eps
+    h = ctypes.c_void_p()
+    st = lib.mg_step_plan_create(ctypes.byref(d), ctypes.byref(h))
+    if st == 0:
+        lib.mg_step_plan_destroy(h)
+    return st, h.value
+
+
+BAD_SETTINGS = {
+    "loss_kind": dict(loss=3),
+    "negative_loss_kind": dict(loss=-1),
+    "precision": dict(precision=2),
+    "optimizer": dict(optimizer=4),
+    "negative_optimizer": dict(optimizer=-1),
+    "adam_beta1_one": dict(optimizer=binding.OPTIMIZERS["adam"], beta1=1.0),
+    "adam_beta2_negative": dict(optimizer=binding.OPTIMIZERS["adam"], beta2=-0.5),
+    "adam_eps_zero": dict(optimizer=binding.OPTIMIZERS["adam"], eps=0.0),
+    "adam_beta_nan": dict(optimizer=binding.OPTIMIZERS["adam"], beta1=float("nan")),
+    "laprop_eps_negative": dict(optimizer=binding.OPTIMIZERS["laprop"], eps=-1e-8),
+    "laprop_beta2_one": dict(optimizer=binding.OPTIMIZERS["laprop"], beta2=1.0),
+    "momentum_one": dict(optimizer=binding.OPTIMIZERS["sgd_momentum"], beta1=1.0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BAD_SETTINGS))
+def test_settings_validation(lib, case):
+    """Out-of-range loss, precision and optimizer settings are rejected at
+    creation, before any device work, and no plan is returned."""
+    st, h = _create_raw(lib, [W.linear(4, 2, False)], **BAD_SETTINGS[case])
+    assert st == binding.MG_ERR_INVALID_ARG
+    assert h is None
+    assert lib.mg_last_error(None)
+
+
+def test_null_plan_in_every_entry_point(lib):
+    """Every call that takes a plan answers a NULL plan with an error status
+    (or zero / NULL), without touching a device."""
+    E = binding.MG_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(64)
+    n = ctypes.c_size_t()
+    assert lib.mg_param_tensor_count(None) == 0
+    assert lib.mg_workspace_bytes(None) == 0
+    assert lib.mg_param_info(None, 0, None, None, None) == E
+    assert lib.mg_loss(None, None, None) == E
+    assert lib.mg_loss_async(None, buf, None) == E
+    assert lib.mg_loss_device_ptr(None) is None
+    assert lib.mg_refresh_params(None, None, None) == E
+    assert lib.mg_plan_dump(None, buf, 64) == 0
+    assert lib.mg_debug_check_finite(None, None, 0, None, None) == E
+    assert lib.mg_last_launch_count(None) == 0
+    assert lib.mg_graph_replays(None) == 0
+    assert lib.mg_profile_begin(None, 1) == E
+    assert lib.mg_profile_end(None) == E
+    assert lib.mg_profile_entries(None) == 0
+    assert lib.mg_profile_entry(None, 0, None, 0, None, None, None, None) == E
+    assert lib.mg_checkpoint_bytes(None, 1, 1) == 0
+    assert lib.mg_checkpoint_save(None, None, None, None, buf, 64, ctypes.byref(n), None) == E
+    assert lib.mg_checkpoint_load(None, buf, 64, None, None, None, None) == E
