@@ -39,8 +39,8 @@ static graph.  Three modes:
 * "strict": every graph value -- each layer's output and the gradient with
   respect to each value -- is stored as float32 (strict f32);
 * "bf16": x, the weight matrices, the MSE target and every graph value and
-  value gradient are stored as bf16 (round to nearest even); the workloads'
-  "bf16 activations/weights, fp32 master weights and Adam moments".
+  value gradient are stored as bf16 (round to nearest even), as the bf16
+  workloads specify, with the master weights and Adam moments in fp32.
 
 Arithmetic inside an op is float64 on the stored operands, rounded once to the
 value type.  Parameter gradients are float64; parameters and Adam moments are

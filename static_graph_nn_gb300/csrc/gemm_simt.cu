@@ -1,8 +1,8 @@
 // Register-blocked CUDA-core GEMM with a fused epilogue.
 //
 // This is the strict-f32 matmul of the library: fp32 operands, fp32 FFMA
-// accumulation, no tensor cores and no TF32 (the pages' "portable scalar
-// matmul" path, README Environment variables section, kept separate from the
+// accumulation, no tensor cores and no TF32 (the scalar f32 matmul the
+// README's Environment variables section describes, kept separate from the
 // reduced-precision tiles as the abstract's strict f32 protocol requires).  It
 // also serves bf16 GEMMs whose widths do not meet the tensor-memory-access
 // alignment rule (a row that is not a multiple of 16 bytes, e.g. 10 classes).
