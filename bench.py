@@ -37,8 +37,6 @@ sys.path.insert(0, ROOT)
 TRAFFIC = {}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (maximum SM clock)
-FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def load_peaks():
@@ -275,132 +273,110 @@ def run_reference(args):
     return 0
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
-    ap.add_argument("--precision", default=None, choices=[None, "strict", "bf16"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    if args.impl == "reference":
-        return run_reference(args)
-
-    import numpy as np
-    import torch
-
-    import __graft_entry__
+def make_plan(w, prec, graph=True):
+    """A plan for the workload; graph=False creates it with the step's graph
+    replay turned off (MG_GRAPH=0, read at plan creation)."""
     from static_graph_nn_gb300 import Plan
-    from static_graph_nn_gb300 import workloads as W
-    from static_graph_nn_gb300.replicas import job_throughput, max_over_ranks
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    if rank == 0 or world == 1:
-        __graft_entry__.build()
-    if dist:
-        dist.barrier()
-    from static_graph_nn_gb300 import binding
-    binding.load()
-
-    w, prec = workload_for(args.config, args.precision)
-    plan = Plan.for_workload(w, prec)
-    p0 = W.init_params(w)
-    flat = torch.zeros(plan.param_count, dtype=torch.float32)
-    for (off, r, c), t in zip(plan.param_info(), p0):
-        flat[off:off + r * c] = torch.from_numpy(t.reshape(-1))
-    params = flat.cuda()
-    grads = torch.zeros_like(params)
-    m = torch.zeros_like(params) if w.optimizer in ("adam", "laprop", "sgd_momentum") else None
-    v = torch.zeros_like(params) if w.optimizer in ("adam", "laprop") else None
-    x = W.make_x(w)
-    y = W.make_labels(w)
-    xt = torch.from_numpy(x)
-    if prec == "bf16":
-        xt = xt.to(torch.bfloat16)
-    yt = torch.from_numpy(y)
-    if w.loss == "mse" and prec == "bf16":
-        yt = yt.to(torch.bfloat16)
-    x_host = xt.contiguous().pin_memory()
-    y_host = yt.contiguous().pin_memory()
-    x_dev = x_host.cuda()
-    y_dev = y_host.cuda()
-    stream = torch.cuda.current_stream()
-    step = 0
-
-    def one_step():
-        nonlocal step
-        step += 1
-        plan.train_step(params, grads, m, v, x_dev, y_dev, w.lr, step, stream)
-
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-
-    # ---- timed region: device-resident inputs, the steps as a user runs
-    # them (from the second call on, each step is a CUDA-graph replay) ----
+    if graph:
+        return Plan.for_workload(w, prec)
+    old = os.environ.get("MG_GRAPH")
+    os.environ["MG_GRAPH"] = "0"
     try:
-        clocks = NvmlSampler(local)
-    except Exception:
-        clocks = ClockSampler(local)
-    clocks.start()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    replays0 = plan.graph_replays()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        one_step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    launches = plan.last_launch_count() * args.steps
-    replays = plan.graph_replays() - replays0
+        return Plan.for_workload(w, prec)
+    finally:
+        if old is None:
+            del os.environ["MG_GRAPH"]
+        else:
+            os.environ["MG_GRAPH"] = old
 
-    # ---- kernel timing: the same K steps again, launched directly with a
-    # CUDA event pair around every kernel on the stream it runs on ----
-    plan.profile_begin(args.steps)
-    ev2 = torch.cuda.Event(enable_timing=True)
-    ev3 = torch.cuda.Event(enable_timing=True)
-    ev2.record(stream)
-    for _ in range(args.steps):
-        one_step()
-    ev3.record(stream)
-    torch.cuda.synchronize()
-    ms_prof = ev2.elapsed_time(ev3)
-    prof = plan.profile_end()
-    clk = clocks.stop()
-    loss = plan.loss(stream)
 
-    # ---- end to end: host buffers, H2D copies and the loss read inside ----
-    # A training loop as a user would pipeline it: every step's inputs are
-    # copied from pinned host memory on a copy stream into one of two device
-    # buffers while the previous step computes, and every step's loss (with
-    # the pipeline's error flag) is copied back and read on the host one step
-    # later, so the copies overlap the compute and the host enqueues the next
-    # step while the GPU runs this one.
-    e2e_steps = max(10, args.steps)
-    e2e_warm = max(4, args.warmup)
+class Session:
+    """One workload's plan and its device and pinned host buffers."""
+
+    def __init__(self, w, prec):
+        import torch
+
+        from static_graph_nn_gb300 import workloads as W
+        self.w, self.prec = w, prec
+        t0 = time.perf_counter()
+        self.plan = make_plan(w, prec)
+        self.create_ms = (time.perf_counter() - t0) * 1e3
+        p0 = W.init_params(w)
+        flat = torch.zeros(self.plan.param_count, dtype=torch.float32)
+        for (off, r, c), t in zip(self.plan.param_info(), p0):
+            flat[off:off + r * c] = torch.from_numpy(t.reshape(-1))
+        self.params = flat.cuda()
+        self.grads = torch.zeros_like(self.params)
+        self.m = torch.zeros_like(self.params) if w.optimizer in ("adam", "laprop", "sgd_momentum") else None
+        self.v = torch.zeros_like(self.params) if w.optimizer in ("adam", "laprop") else None
+        xt = torch.from_numpy(W.make_x(w))
+        if prec == "bf16":
+            xt = xt.to(torch.bfloat16)
+        yt = torch.from_numpy(W.make_labels(w))
+        if w.loss == "mse" and prec == "bf16":
+            yt = yt.to(torch.bfloat16)
+        self.x_host = xt.contiguous().pin_memory()
+        self.y_host = yt.contiguous().pin_memory()
+        self.x_dev = self.x_host.cuda()
+        self.y_dev = self.y_host.cuda()
+        self.stream = torch.cuda.current_stream()
+        self.step = 0
+
+    def one_step(self, plan=None, x=None, y=None):
+        self.step += 1
+        (plan or self.plan).train_step(self.params, self.grads, self.m, self.v,
+                                       self.x_dev if x is None else x,
+                                       self.y_dev if y is None else y, self.w.lr, self.step,
+                                       self.stream)
+
+    def close(self):
+        self.plan.close()
+
+
+def time_reps(sess, plan, steps, reps, dist):
+    """reps timed regions of `steps` steps each (device-resident inputs, CUDA
+    events on the launching stream, a barrier and a synchronize on both
+    sides); milliseconds per region."""
+    import torch
+    out = []
+    for _ in range(reps):
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(sess.stream)
+        for _ in range(steps):
+            sess.one_step(plan)
+        ev1.record(sess.stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        out.append(ev0.elapsed_time(ev1))
+    return out
+
+
+def time_e2e(sess, steps, warmup, dist):
+    """Seconds per step end to end: a training loop as a user pipelines it.
+    Every step's inputs are copied from pinned host memory on a copy stream
+    into one of two device buffers while the previous step computes, and every
+    step's loss (with the pipeline's error flag) is copied back and read on the
+    host one step later, so the copies overlap the compute and the host
+    enqueues the next step while the GPU runs this one."""
+    import torch
+    plan, stream = sess.plan, sess.stream
+    e2e_steps = max(10, steps)
+    e2e_warm = max(4, warmup)
     total = e2e_warm + e2e_steps
     copy_stream = torch.cuda.Stream()
-    xb = [x_dev, torch.empty_like(x_dev)]
-    yb = [y_dev, torch.empty_like(y_dev)]
+    xb = [sess.x_dev, torch.empty_like(sess.x_dev)]
+    yb = [sess.y_dev, torch.empty_like(sess.y_dev)]
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(total)]
     loss_host = torch.zeros(total, 2, dtype=torch.float32).pin_memory()
-    e2e_losses = []
-
+    losses = []
+    x_host, y_host = sess.x_host, sess.y_host
     # inputs under 1 MiB are copied on the compute stream itself: their copy is
     # shorter than the cross-stream synchronisation it would overlap with
     overlap = (x_host.numel() * x_host.element_size() + y_host.numel() * y_host.element_size()
@@ -419,7 +395,6 @@ def main():
 
     # the loop's first e2e_warm steps are untimed warm-up (each buffer's step
     # graph is captured on its second use); the clock starts at the step after
-    # (that step's input copy is enqueued after the clock starts)
     t0 = None
     enqueue_copy(0)
     for t in range(total):
@@ -437,31 +412,97 @@ def main():
         else:
             xb[b].copy_(x_host, non_blocking=True)    # on the compute stream
             yb[b].copy_(y_host, non_blocking=True)
-        step += 1
-        plan.train_step(params, grads, m, v, xb[b], yb[b], w.lr, step, stream)
+        sess.one_step(plan, xb[b], yb[b])
         if overlap:
             consumed[b].record(stream)
         plan.loss_async(loss_host[t].data_ptr(), stream)
         done[t].record(stream)
         if t > e2e_warm:
             done[t - 1].synchronize()
-            e2e_losses.append(float(loss_host[t - 1, 0]))
+            losses.append(float(loss_host[t - 1, 0]))
     done[total - 1].synchronize()
-    e2e_losses.append(float(loss_host[total - 1, 0]))
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if any(loss_host.view(torch.int32)[:, 1].tolist()) or not all(map(math.isfinite, e2e_losses)):
+    losses.append(float(loss_host[total - 1, 0]))
+    sec = (time.perf_counter() - t0) / e2e_steps
+    if any(loss_host.view(torch.int32)[:, 1].tolist()) or not all(map(math.isfinite, losses)):
         raise RuntimeError("end-to-end steps reported a timed-out pipeline or a non-finite loss")
+    h2d = x_host.numel() * x_host.element_size() + y_host.numel() * y_host.element_size()
+    return sec, h2d
 
-    ms, e2e_s = max_over_ranks([ms, e2e_s], device="cuda")
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return 0
 
+def pick_peak(prec, peaks, peak_src, clk, ffma):
+    """The roofline denominator: the strict path's measured FFMA rate; for bf16
+    the measured burst peak when the timed region ran at full clock with no
+    power cap (short steps between idle gaps), the sustained peak otherwise."""
+    if prec != "bf16":
+        return "alu", "TFLOP/s", ffma, "FP32 FFMA peak measured by mg_ffma_peak in this run"
+    capped = "sw_power_cap" in (clk.get("reasons") or []) or (
+        clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"])
+    if capped:
+        return ("tensor", "TFLOP/s", peaks.get("bf16_tflops_sustained", 1700.0),
+                f"sustained bf16 peak ({peak_src}): the timed region ran power-capped or below "
+                f"95% of the maximum SM clock")
+    return ("tensor", "TFLOP/s", peaks.get("bf16_tflops", 1900.0),
+            f"burst bf16 peak ({peak_src}): the timed region ran at full clock with no power cap")
+
+
+def measure(w, prec, args, dist, world, rank, local, peaks, peak_src, ffma, reps=5):
+    """Everything the JSON line reports for one workload."""
+    import torch
+
+    from static_graph_nn_gb300.replicas import job_throughput, max_over_ranks
+    sess = Session(w, prec)
+    for _ in range(args.warmup):
+        sess.one_step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs, the steps as a user runs
+    # them (from the second call on, each step is a CUDA-graph replay);
+    # `reps` repetitions, the median reported ----
+    try:
+        clocks = NvmlSampler(local)
+    except Exception:
+        clocks = ClockSampler(local)
+    clocks.start()
+    replays0 = sess.plan.graph_replays()
+    first = time_reps(sess, sess.plan, args.steps, 1, dist)
+    replays = sess.plan.graph_replays() - replays0
+    launches = sess.plan.last_launch_count() * args.steps
+    clk = clocks.stop()
+    # the measurement protocol's repetitions: the first region and `reps` - 1
+    # more, with graph replay, then `reps` with every kernel launched directly
+    reps_graph = first + time_reps(sess, sess.plan, args.steps, reps - 1, dist)
+
+    # the same repetitions with every kernel launched directly (a second plan
+    # created with graph replay off, on the same buffers)
+    plan_ng = make_plan(w, prec, graph=False)
+    for _ in range(2):
+        sess.one_step(plan_ng)
+    reps_direct = time_reps(sess, plan_ng, args.steps, reps, dist)
+    plan_ng.close()
+
+    # ---- kernel timing: the same K steps again, launched directly with a
+    # CUDA event pair around every kernel on the stream it runs on ----
+    sess.plan.profile_begin(args.steps)
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    ev2.record(sess.stream)
+    for _ in range(args.steps):
+        sess.one_step()
+    ev3.record(sess.stream)
+    torch.cuda.synchronize()
+    ms_prof = ev2.elapsed_time(ev3)
+    prof = sess.plan.profile_end()
+    loss = sess.plan.loss(sess.stream)
+
+    e2e_s, h2d = time_e2e(sess, args.steps, args.warmup, dist)
+
+    ms = first[0]
+    ms_med = statistics.median(reps_graph)
+    ms_direct = statistics.median(reps_direct)
+    ms, ms_med, ms_direct, e2e_s = max_over_ranks([ms, ms_med, ms_direct, e2e_s], device="cuda")
     ms_step = ms / args.steps
     flops = w.flops_per_step()
-    peaks, peak_src = load_peaks()
-    bf16_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0))
+    bound, unit, peak, peak_note = pick_peak(prec, peaks, peak_src, clk, ffma)
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
 
     # dominant kernel: schedule entries grouped by the kernel they launch (the
@@ -477,13 +518,9 @@ def main():
         f["bytes"] += e["bytes"] * e["launches"]
     top = max(fam.values(), key=lambda f: f["total_ms"])
     if top["flops"] > 0:
-        if prec == "bf16":
-            bound, unit, peak = "tensor", "TFLOP/s", bf16_peak
-        else:
-            bound, unit, peak = "alu", "TFLOP/s", FP32_FFMA_TFLOPS
         achieved = top["flops"] / (top["total_ms"] * 1e-3) / 1e12
     else:
-        bound, unit, peak = "hbm", "GB/s", hbm_peak
+        bound, unit, peak, peak_note = "hbm", "GB/s", hbm_peak, f"HBM copy bandwidth ({peak_src})"
         achieved = top["bytes"] / (top["total_ms"] * 1e-3) / 1e9
     total_prof = sum(e["total_ms"] for e in prof)
     kernels = [{"name": e["name"], "share": e["total_ms"] / total_prof if total_prof else None,
@@ -493,27 +530,30 @@ def main():
                 "gbs": (e["bytes"] / (e["total_ms"] / max(1, e["launches"]) * 1e-3) / 1e9)
                 if e["total_ms"] else None}
                for e in sorted(prof, key=lambda e: -e["total_ms"])[:8]]
-
-    value = job_throughput(world, args.steps, ms * 1e-3)
-    h2d = x_host.numel() * x_host.element_size() + y_host.numel() * y_host.element_size()
-    line = {
-        "metric": "training steps/s (achieved TFLOP/s per step)",
-        "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": prec if prec == "bf16" else "f32",
-        "data": "synthetic",
+    out = {
+        "value": job_throughput(world, args.steps, ms * 1e-3),
+        "ms_per_step": ms_step,
+        "dtype": prec if prec == "bf16" else "f32",
         "config": {"workload": w.name, "batch": w.batch, "precision": prec,
                    "optimizer": w.optimizer, "flops_per_step": flops,
                    "parallelism": f"replicas x{world}",
-                   "l2": "working set per step >> 129 MB L2 (weights, activations, Adam state)"},
+                   "l2": "working set per step >> 129 MB L2 (weights, activations, optimizer "
+                         "state); no flush between steps"},
         "tflops": flops / (ms_step * 1e-3) / 1e12,
-        "pct_of_peak": flops / (ms_step * 1e-3) / 1e12 / (bf16_peak if prec == "bf16" else FP32_FFMA_TFLOPS),
-        "peak_source": peak_src,
+        "pct_of_peak": flops / (ms_step * 1e-3) / 1e12 / peak if bound != "hbm" else None,
         "roofline": {"kernel": top["name"], "launches_timed": top["launches"],
                      "share": top["total_ms"] / total_prof if total_prof else None,
                      "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "traffic": TRAFFIC.get((w.name, top["name"])),
-                     "peak_note": f"{'sustained bf16' if bound == 'tensor' else bound} peak, {peak_src}"},
+                     "unit": unit, "frac": achieved / peak,
+                     "traffic": TRAFFIC.get((w.name, top["name"])),
+                     "peak_note": peak_note},
+        "repetitions": {"how": f"{reps} timed regions of {args.steps} steps each, back to back, "
+                               f"with graph replay (the first is the headline region) and "
+                               f"with every kernel launched directly; medians",
+                        "graph_ms_per_step": [r / args.steps for r in reps_graph],
+                        "direct_ms_per_step": [r / args.steps for r in reps_direct],
+                        "graph_median_value": job_throughput(world, args.steps, ms_med * 1e-3),
+                        "direct_median_value": job_throughput(world, args.steps, ms_direct * 1e-3)},
         "kernels": kernels,
         "kernel_families": [{"kernel": f["name"], "launches": f["launches"],
                              "share": f["total_ms"] / total_prof if total_prof else None,
@@ -527,10 +567,102 @@ def main():
                                  "CUDA event pair around every kernel (roofline and kernels)"},
         "loss": loss,
         "clocks": clk,
-        "e2e": {"value": job_throughput(world, 1, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 8},
-        "plan_workspace_bytes": plan.workspace_bytes,
+        "e2e": {"value": job_throughput(world, 1, e2e_s), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8},
+        "plan_workspace_bytes": sess.plan.workspace_bytes,
+        "plan_create_ms": sess.create_ms,
     }
+    sess.close()
+    return out
+
+
+def plan_create_times(reps=3):
+    """Wall time of mg_step_plan_create (validation, layout, schedule, the
+    workspace allocation) for every workload, the median of `reps`; the
+    pages' counterpart is the session's compile time."""
+    from static_graph_nn_gb300 import Plan
+    from static_graph_nn_gb300 import workloads as W
+    out = {}
+    for key in ("c1", "c2", "c3", "c4", "c5"):
+        w = W.workload(key)
+        for prec in w.precisions:
+            ts = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                p = Plan.for_workload(w, prec)
+                ts.append((time.perf_counter() - t0) * 1e3)
+                p.close()
+            out[f"{w.name}/{prec}"] = statistics.median(ts)
+    return out
+
+
+EXTRA = {"c3": ("c5", "c4")}   # the default run also times these after the headline
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c3", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--precision", default=None, choices=[None, "strict", "bf16"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --config (the default run adds the attention and "
+                         "residual-network workloads after the large MLP)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import __graft_entry__
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    from static_graph_nn_gb300 import binding
+    binding.load()
+
+    peaks, peak_src = load_peaks()
+    w, prec = workload_for(args.config, args.precision)
+    ffma = binding.ffma_peak()[0] if prec != "bf16" else None
+    head = measure(w, prec, args, dist, world, rank, local, peaks, peak_src, ffma)
+    extras = {}
+    if not args.no_extra and args.precision in (None, "bf16"):
+        for key in EXTRA.get(args.config, ()):
+            we, pe = workload_for(key, None)
+            extras[we.name] = measure(we, pe, args, dist, world, rank, local, peaks, peak_src, None)
+    creates = plan_create_times()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    line = {
+        "metric": "training steps/s (achieved TFLOP/s per step)",
+        "value": head["value"], "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+        "config": head["config"], "roofline": head["roofline"], "clocks": head["clocks"],
+        "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "peak_source": peak_src,
+    }
+    for k, v in head.items():
+        line.setdefault(k, v)
+    if ffma is not None:
+        line["ffma_peak_tflops"] = ffma
+    line["plan_create_ms"] = {"this_workload": head["plan_create_ms"], "all": creates,
+                              "pages_compile_s": "0.1-2.4 (consumer GPUs, Vulkan/Metal)"}
+    if extras:
+        line["configs"] = extras
     if not args.no_cpu_baseline and world == 1:
         sec, rows, threads = cpu_oracle_sample(w, prec)
         line["cpu_baseline"] = {"value": 1.0 / sec, "unit": "steps/s", "cores": threads,
@@ -538,7 +670,6 @@ def main():
                                 "sample": f"one oracle step on {rows} of {w.batch} rows, "
                                           f"time scaled by rows"}
     print(json.dumps(line), flush=True)
-    plan.close()
     if dist:
         dist.destroy_process_group()
     return 0

@@ -101,30 +101,46 @@ typedef struct {
  * typed static graph of the README's Example section, with its shapes fixed. */
 mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out);
 
-/* Free the workspace.  NULL is a no-op.  Synchronises the device first. */
+/* Free the workspace.  NULL is a no-op.  Synchronises the device first.
+ * (The session that build_session returns owns its device buffers for its
+ * lifetime: "Meganeura" README, Example section.) */
 void mg_step_plan_destroy(mg_plan* plan);
 
-/* Floats in each of the flat parameter / gradient / moment buffers. */
+/* Floats in each of the flat parameter / gradient / moment buffers (the
+ * parameter nodes of the README's Example section, packed). */
 size_t mg_param_count(const mg_plan* plan);
 
-/* Number of parameter tensors (W, b, gamma in declaration order). */
+/* Number of parameter tensors (W, b, gamma in declaration order): the graph's
+ * parameter nodes ("Meganeura" README, Example section). */
 int mg_param_tensor_count(const mg_plan* plan);
 
 /* Tensor i of the flat buffers: element offset, logical rows and cols (a
  * vector has rows = 1).  Offsets are multiples of 64 elements; the gaps
- * between tensors are never read or written. */
+ * between tensors are never read or written.  The logical shape is the one a
+ * checkpoint stores, without device padding ("Meganeura" README, Contents
+ * section, checkpoint notes). */
 mg_status mg_param_info(const mg_plan* plan, int i, size_t* offset, int* rows, int* cols);
 
-/* Bytes of device workspace the plan owns. */
+/* Bytes of device workspace the plan owns, after the memory planner's
+ * lifetime sharing of gradient buffers (abstract of "Meganeura: Portable GPU
+ * Training and Inference through Vulkan and Metal": memory planner; README,
+ * Environment variables section: buffer lifetime aliasing, off with
+ * MG_NO_ALIAS=1 here). */
 size_t mg_workspace_bytes(const mg_plan* plan);
 
-/* Forward pass only.  params: flat fp32 [mg_param_count]; x: [batch, d_in],
- * fp32 in strict mode, bf16 in bf16 mode; out: fp32 [batch, d_out] (logits or
- * the model output), written row-major. */
+/* Forward pass only: the inference side of the train-to-deploy stack (README,
+ * Contents section: a trained model reloaded into a fresh inference session;
+ * abstract: one graph and runtime for training and deployed inference).
+ * params: flat fp32 [mg_param_count]; x: [batch, d_in], fp32 in strict mode,
+ * bf16 in bf16 mode; out: fp32 [batch, d_out] (logits or the model output),
+ * written row-major; in bf16 mode each output value is the bf16 value the
+ * graph stores, widened. */
 mg_status mg_forward(mg_plan* plan, const float* params, const void* x, float* out,
                      mg_stream_t stream);
 
-/* One full training step: forward, loss, backward, optimizer update.
+/* One full training step: forward, loss, backward, optimizer update (README,
+ * Example section: the Trainer's step over the session; Contents section: SGD
+ * and Adam; abstract: automatic differentiation and optimizer).
  *  params  fp32 [P]  updated in place (fp32 master weights)
  *  grads   fp32 [P]  overwritten with dLoss/dparams of this step (before the update)
  *  adam_m, adam_v fp32 [P]  optimizer state, updated in place: Adam and LaProp
@@ -151,7 +167,8 @@ mg_status mg_train_step(mg_plan* plan, float* params, float* grads, float* adam_
                         float* adam_v, const void* x, const void* labels, float lr, int step,
                         mg_stream_t stream);
 
-/* Copy the last step's loss to the host; synchronises `stream`. */
+/* Copy the last step's loss (the batch mean the README's Example section
+ * prints per step) to the host; synchronises `stream`. */
 mg_status mg_loss(mg_plan* plan, float* host_loss, mg_stream_t stream);
 
 /* Enqueue, without waiting, a copy of the last step's loss and the plan's
@@ -163,11 +180,14 @@ mg_status mg_loss(mg_plan* plan, float* host_loss, mg_stream_t stream);
  * loops that enqueue the next step before reading this one's loss. */
 mg_status mg_loss_async(mg_plan* plan, void* host_dst, mg_stream_t stream);
 
-/* Device address of the last step's loss (one fp32), valid until destroy. */
+/* Device address of the last step's loss (one fp32, the batch mean of the
+ * README's Example section), valid until destroy. */
 const float* mg_loss_device_ptr(const mg_plan* plan);
 
 /* Re-derive the bf16 weight copy from params (after the caller changed them,
- * e.g. a checkpoint restore).  A no-op in strict mode. */
+ * e.g. a checkpoint restore).  A no-op in strict mode.  The copy is the
+ * reduced-precision operand of the validated fast path, kept apart from the
+ * strict f32 path (abstract; README, Environment variables section). */
 mg_status mg_refresh_params(mg_plan* plan, const float* params, mg_stream_t stream);
 
 /* ---- checkpoints --------------------------------------------------------
@@ -200,26 +220,37 @@ mg_status mg_checkpoint_load(mg_plan* plan, const void* host_buf, size_t len, fl
                              float* m, float* v, mg_stream_t stream);
 
 /* Human-readable schedule: one line per kernel with its shapes and the
- * workspace offsets (the analogue of the pages' plan dump).  Writes at most
- * cap bytes including the terminating NUL; returns the full length. */
+ * workspace offsets: the dispatch order and alias map that the README's plan
+ * dump switch prints at build (Environment variables section).  Writes at
+ * most cap bytes including the terminating NUL; returns the full length. */
 size_t mg_plan_dump(const mg_plan* plan, char* buf, size_t cap);
 
-/* Message of the last failure; NULL plan gives the process-wide message. */
+/* Message of the last failure; NULL plan gives the process-wide message.
+ * (The pages have no counterpart: this is the ABI's error convention, in
+ * place of the Rust API's panics and structured errors.) */
 const char* mg_last_error(const mg_plan* plan);
 
 /* Scan n floats (device) for NaN/Inf; synchronises stream.  Returns
- * MG_ERR_NONFINITE and the first bad index in *first_bad (may be NULL). */
+ * MG_ERR_NONFINITE and the first bad index in *first_bad (may be NULL).  The
+ * debug session's scan for the first NaN/Inf after a step ("Meganeura"
+ * README, Debugging section). */
 mg_status mg_debug_check_finite(mg_plan* plan, const float* data, size_t n, long long* first_bad,
                                 mg_stream_t stream);
 
 /* Kernels launched by the last mg_train_step / mg_forward call (a replayed
- * step counts the kernels its graph holds). */
+ * step counts the kernels its graph holds): the dispatch count of the
+ * README's per-dispatch profile (Profiling section). */
 int mg_last_launch_count(const mg_plan* plan);
 
-/* mg_train_step calls served by a graph replay since the plan was created. */
+/* mg_train_step calls served by a graph replay since the plan was created.
+ * The step is compiled once and its fixed command list submitted every step
+ * (README, Example section: build_session compiles once); here that list is
+ * a CUDA graph. */
 long long mg_graph_replays(const mg_plan* plan);
 
 /* ---- per-kernel timing (CUDA events around each launch) ----------------
+ * The per-dispatch timing profile of the README's Profiling section, with
+ * CUDA events in place of hardware timestamp queries.
  * mg_profile_begin(plan, max_calls): from now on, each mg_train_step records
  * a start/stop event pair around every kernel, for up to max_calls calls.
  * mg_profile_end: synchronises, sums the elapsed time per schedule entry and
@@ -231,6 +262,17 @@ mg_status mg_profile_end(mg_plan* plan);
 int mg_profile_entries(const mg_plan* plan);
 mg_status mg_profile_entry(const mg_plan* plan, int i, char* name, size_t name_cap,
                            int* launches, double* total_ms, double* flops, double* bytes);
+
+/* ---- measurement ---------------------------------------------------------
+ * The pages have no counterpart to this call: it measures the roofline
+ * denominator of the strict-f32 path, whose matrix products run on the FP32
+ * FFMA units only (the strict scalar matmul of the "Meganeura" README,
+ * Environment variables section).  Runs a fused multiply-add kernel on every
+ * SM of the current device for a few milliseconds, synchronises `stream`,
+ * and writes the achieved FP32 TFLOP/s (2 flop per FFMA) to *tflops and the
+ * FFMA flop per clock per SM to *flop_per_clk_per_sm (may be NULL).  It
+ * allocates and frees a few bytes of device memory. */
+mg_status mg_ffma_peak(double* tflops, double* flop_per_clk_per_sm, mg_stream_t stream);
 
 /* ---- softmax cross-entropy without device allocation -----------------
  * The Meganeura pages have no counterpart to this call.  It is for callers
@@ -251,11 +293,15 @@ mg_status mg_profile_entry(const mg_plan* plan, int i, char* name, size_t name_c
  * Scratch: the per-row losses go to a fixed array in the library's device
  * memory of 65536 floats (256 KB), held by every GPU that loads the library
  * until the process exits.  rows above 65536 return MG_ERR_INVALID_ARG.  The
- * first call on a device looks up that array's device address (with that
- * device current); make that first call before any stream capture.  All calls
- * share the array: calls that overlap on the GPU (different streams, or
- * different host threads) race and give wrong results.  Each call overwrites
- * the slots it reads, so nothing needs clearing between calls. */
+ * first call in each device context (the first call on a device, and the
+ * first after a cudaDeviceReset re-creates the context) looks up that array's
+ * device address with that device current; make that first call before any
+ * stream capture.  All calls share the array: calls that overlap on the GPU
+ * (different streams, or different host threads) race and give wrong results.
+ * Each call overwrites the slots it reads, so nothing needs clearing between
+ * calls.  A CUDA error already pending on the calling thread is returned as
+ * MG_ERR_CUDA (the message says it came before the call) and nothing is
+ * launched; launch failures carry the CUDA error string in the message. */
 mg_status mg_softmax_ce_noalloc(int dtype, const void* logits, int rows, int cols, int label_kind,
                                 const void* labels, void* dlogits, float* loss, mg_stream_t stream);
 

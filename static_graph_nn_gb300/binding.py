@@ -63,6 +63,8 @@ _SIGS = {
     "mg_profile_begin": (ctypes.c_int, [_P, ctypes.c_int]),
     "mg_profile_end": (ctypes.c_int, [_P]),
     "mg_profile_entries": (ctypes.c_int, [_P]),
+    "mg_ffma_peak": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                    _P]),
     "mg_softmax_ce_noalloc": (ctypes.c_int, [ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, _P, _P, _P, _P]),
     "mg_checkpoint_bytes": (ctypes.c_size_t, [_P, ctypes.c_int, ctypes.c_int]),
@@ -266,3 +268,14 @@ class Plan:
             out.append({"name": name.value.decode(), "launches": n.value, "total_ms": ms.value,
                         "flops": fl.value, "bytes": by.value})
         return out
+
+
+def ffma_peak(stream=None) -> tuple[float, float]:
+    """Measured FP32 FFMA rate of the current device: (TFLOP/s, flop per clock
+    per SM), the strict path's roofline denominator."""
+    lib = load()
+    t, c = ctypes.c_double(), ctypes.c_double()
+    st = lib.mg_ffma_peak(ctypes.byref(t), ctypes.byref(c), _stream(stream))
+    if st != MG_OK:
+        raise MGError(st, lib.mg_last_error(None).decode())
+    return t.value, c.value

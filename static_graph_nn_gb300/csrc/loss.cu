@@ -2,6 +2,9 @@
 // error (+ its gradient), the reduction archetype of the Meganeura README
 // (Example section: cross_entropy_loss(logits, labels) with a dense [B, C]
 // label tensor; "Why Meganeura" section: the reduction kernel archetype).
+#include <cuda.h>
+
+#include <cstdio>
 #include <mutex>
 
 #include "../../include/mg.h"
@@ -361,9 +364,45 @@ namespace {
 constexpr int kNoAllocMaxRows = 65536;
 __device__ __align__(256) float g_noalloc_row_loss[kNoAllocMaxRows];
 
+// The array's device address is looked up once per device context and kept
+// with that context's id: a cudaDeviceReset (or any re-creation of the
+// primary context) loads the module again, possibly at another address, and
+// the new context has a new id, so the address is looked up again.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  float* ptr;
+};
+
 std::mutex g_noalloc_mu;
 constexpr int kMaxDevices = 256;
-float* g_noalloc_scratch[kMaxDevices] = {};   // device address of the array, per device
+ScratchSlot g_noalloc_scratch[kMaxDevices] = {};   // per device: context id, device address
+
+// Id of the calling thread's current context; false when there is none yet
+// or the driver lacks the calls.
+bool current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked_up = true;
+  }
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -383,35 +422,59 @@ extern "C" mg_status mg_softmax_ce_noalloc(int dtype, const void* logits, int ro
     set_global_error("mg_softmax_ce_noalloc: rows must be in [1, 65536] and cols >= 1");
     return MG_ERR_INVALID_ARG;
   }
+  char msg[256];
+  // An error left pending by earlier work on this thread is reported as such,
+  // not as a failure of this call's launches (and nothing is launched).
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) {
+    snprintf(msg, sizeof msg,
+             "mg_softmax_ce_noalloc: a CUDA error was already pending before the call (%s); "
+             "nothing launched", cudaGetErrorString(e));
+    set_global_error(msg);
+    return MG_ERR_CUDA;
+  }
   int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     set_global_error("mg_softmax_ce_noalloc: no usable current CUDA device");
     return MG_ERR_CUDA;
   }
   float* scratch = nullptr;
   {
-    // First call on this device: look up the array's device address (host
-    // code cannot use the array's name as a device pointer).
+    // Set-up on the first call in each device context: look up the array's
+    // device address (host code cannot use the array's name as a device
+    // pointer).
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_scratch[dev]) {
+    unsigned long long id = 0;
+    const bool have_id = current_ctx_id(&id);
+    ScratchSlot& slot = g_noalloc_scratch[dev];
+    if (!have_id || !slot.ptr || slot.ctx_id != id) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_row_loss);
       if (e != cudaSuccess || !p) {
         cudaGetLastError();
-        set_global_error("mg_softmax_ce_noalloc: cudaGetSymbolAddress failed");
+        snprintf(msg, sizeof msg, "mg_softmax_ce_noalloc: cudaGetSymbolAddress failed (%s)",
+                 cudaGetErrorString(e));
+        set_global_error(msg);
         return MG_ERR_CUDA;
       }
-      g_noalloc_scratch[dev] = static_cast<float*>(p);
+      // the lookup made the context current if it was not yet
+      slot.ptr = static_cast<float*>(p);
+      slot.ctx_id = current_ctx_id(&id) ? id : 0;
+      if (!slot.ctx_id) slot.ptr = nullptr;   // no id to key it on: look it up every call
+      scratch = static_cast<float*>(p);
+    } else {
+      scratch = slot.ptr;
     }
-    scratch = g_noalloc_scratch[dev];
   }
   // Every row's slot is written before the reduction reads it, so the array
   // needs no clearing between calls.
   e = ce_loss(dtype == 1 ? DT_BF16 : DT_F32, logits, rows, cols, cols, label_kind, labels,
               dlogits, scratch, loss, (cudaStream_t)stream);
   if (e != cudaSuccess) {
-    set_global_error("mg_softmax_ce_noalloc: kernel launch failed");
+    snprintf(msg, sizeof msg, "mg_softmax_ce_noalloc: kernel launch failed (%s)",
+             cudaGetErrorString(e));
+    set_global_error(msg);
     return MG_ERR_CUDA;
   }
   return MG_OK;

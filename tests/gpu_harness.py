@@ -25,6 +25,14 @@ from static_graph_nn_gb300 import workloads as W
 STRICT_TOL = 1e-4
 BF16_LOSS_TOL = 1e-2
 BF16_COSINE = 0.999
+# Strict mode: updated parameters that miss the plain gate max|a-b| / max|b|
+# <= 1e-4 are allowed only within the band the gradient gate leaves open (see
+# update_band), and only for a few elements of each tensor: at most 10 per
+# million plus 4 (the elements whose gradient lies within the gradient gate of
+# zero, where a normalised update can take either sign; measured on GB300: 4
+# of 18.6M over C2's ten strict steps).
+BAND_FRACTION = 1e-5
+BAND_SLACK = 4
 
 
 def to_device_inputs(w, precision):
@@ -173,7 +181,7 @@ def compare(w, precision, steps):
     dev = Device(plan, w, precision)
     state = (p0, None, None)
     worst = {"loss": 0.0, "grads": 0.0 if precision == "strict" else 1.0, "params": 0.0,
-             "curve": 0.0}
+             "curve": 0.0, "params_plain": 0.0, "band_elems": 0, "elems": 0}
     for t in range(1, steps + 1):
         o = ho[t - 1]
         dev.load(*state)
@@ -201,6 +209,14 @@ def compare(w, precision, steps):
                 e = float(max(excess.max(), 0.0) / max(np.abs(pb).max(), 1e-30))
                 worst["params"] = max(worst["params"], e)
                 assert e <= STRICT_TOL, f"step {t}: param {n} max rel err {e:.3g} beyond band"
+                # the plain gate, and the elements that needed the band to pass it
+                plain = max_rel(pa, pb)
+                outside = int((np.abs(pa - pb) > STRICT_TOL * np.abs(pb).max() + ulp).sum())
+                worst["params_plain"] = max(worst["params_plain"], plain)
+                worst["band_elems"] += outside
+                worst["elems"] += pa.size
+                assert outside <= BAND_FRACTION * pa.size + BAND_SLACK, \
+                    f"step {t}: param {n}: {outside} of {pa.size} elements outside the plain gate"
                 for part, key in ((1, "adam_m"), (2, "adam_v")):
                     if key not in g:
                         continue
@@ -209,6 +225,7 @@ def compare(w, precision, steps):
                     excess = np.abs(ma - mb) - bandk - np.abs(mb) * 2.0 ** -22
                     e = float(max(excess.max(), 0.0) / max(np.abs(mb).max(), 1e-30))
                     assert e <= STRICT_TOL, f"step {t}: {key} {n} max rel err {e:.3g}"
+                    worst[key + "_plain"] = max(worst.get(key + "_plain", 0.0), max_rel(ma, mb))
             else:
                 c = cosine(a, b)
                 worst["grads"] = min(worst["grads"], c)
