@@ -8,10 +8,11 @@
 // D_i = sum_c dO_ic O_ic:  P = exp(S - LSE), dP = dO V^T, dS = P (dP - D),
 // dV = P^T dO, dK = dS^T Q / 8, dQ = dS K / 8.
 //
-// Forward: persistent, one CTA per SM over (query block, head, sequence)
-// units; S, P and O live in tensor memory (P is the A operand of P V, read from
-// TMEM) and two softmax groups take alternate key blocks with their own
-// running maximum and sum, merged at the end of the unit (see below).
+// Forward: persistent, one CTA per SM over (pair of query blocks, head,
+// sequence) units; S, P and O live in tensor memory (P is the A operand of
+// P V, read from TMEM); each of two softmax groups owns one query tile of the
+// pair, and each group's products have an MMA-issuing thread of their own
+// (see below).
 // Backward: the same persistent plan for the dK/dV kernel (per key block,
 // over the query blocks that see it: S^T and dP^T with the keys as the M
 // dimension, P^T and dS^T into TMEM, dV += P^T dO_i and dK += dS^T Q_i) and
@@ -99,6 +100,11 @@ __device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) {
   return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+  __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<uint32_t*>(&hv);
+}
+
 // 2^x for two lanes on the FMA and integer pipes, which the special-function
 // unit's ex2 leaves idle: 2^x = 2^j 2^f with j = round(x) (adding 1.5 * 2^23
 // rounds to an integer and leaves j in the low mantissa bits), f = x - j in
@@ -122,45 +128,6 @@ __device__ __forceinline__ float2 ex2_poly2(float2 x) {
                      __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
 }
 
-constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
-constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
-
-// ============================================================ forward
-// Persistent, one CTA per SM; a work unit is one 128-row query block of one
-// (head, sequence), dealt to the CTAs heaviest first in snake order.  Warp 8
-// is the TMA producer, warp 9 issues the MMAs, warps 0-7 do the softmax in
-// two groups: group p (warps 4p .. 4p+3, one query row per thread) takes the
-// key blocks whose running index g has parity p, with its own buffers
-//   S[p] = Q K_g^T            TMEM, fp32, 128 columns
-//   P[p] = 2^(S/8 log2e - m)  TMEM, bf16 pairs, 64 columns
-//   O[p] += P[p] V_g          TMEM, fp32, 64 columns (A operand read from TMEM)
-// and its own running maximum m and sum l, so the two groups never wait for
-// each other inside a unit (their warps share the SM sub-partitions and fill
-// each other's latencies).  At the end of a unit the two partial results are
-// merged: M = max(m0, m1), O = (O0 2^(m0-M) + O1 2^(m1-M)) / (l0 2^(m0-M) +
-// l1 2^(m1-M)).  m is a reference maximum in log2 units; it is raised, and
-// O[p] and l rescaled, only when a block's maximum exceeds it by more than 8,
-// so that P <= 2^8.
-constexpr int FWD_THREADS = 320;
-constexpr int FWD_NST = 3;                                  // K/V ring stages
-constexpr uint32_t F_S = 0, F_P = 256, F_O = 384;           // TMEM columns of S[0], P[0], O[0]
-constexpr float RESCALE_T = 8.0f;
-
-struct FwdUnit {
-  int qb, h, b;   // query block, head, sequence; key blocks 0 .. qb
-};
-
-__device__ __forceinline__ bool fwd_unit(int k, int n_units, int nqb, int H, FwdUnit& U) {
-  const int G = gridDim.x;
-  const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-  if (u >= n_units) return false;
-  const int hb = n_units / nqb;
-  U.qb = nqb - 1 - u / hb;
-  U.h = (u % hb) % H;
-  U.b = (u % hb) / H;
-  return true;
-}
-
 // 32 fp32 S values (raw bits) of row r at columns col0.. : keys after the
 // query get -inf when the block is the diagonal one.
 __device__ __forceinline__ void mask_diag(uint32_t (&v)[32], int col0, int r) {
@@ -169,43 +136,100 @@ __device__ __forceinline__ void mask_diag(uint32_t (&v)[32], int col0, int r) {
     if (col0 + e > r) v[e] = 0xff800000u;
 }
 
-// Barrier between the two warps that share a TMEM lane quarter (ids 1-4).
-__device__ __forceinline__ void pair_sync(int quarter) {
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+constexpr uint32_t IDESC_128x128_KK = instr_desc(128, 128, 0, 0);
+constexpr uint32_t IDESC_128x64_KMN = instr_desc(128, 64, 0, 1);
+
+// ============================================================ forward
+// Persistent, one CTA per SM.  A work unit is one (sequence b, head h, pair of
+// adjacent 128-row query blocks 2p, 2p+1), dealt to the CTAs heaviest first
+// in snake order; the two query tiles share every K/V tile the CTA loads.
+// Softmax group g (warps 4g .. 4g+3, one query row per thread) owns one of
+// the two tiles -- the groups take the higher block of the pair in turn, so
+// their work over a run balances -- with its own buffers
+//   S[g] = Q_g K_j^T           TMEM, fp32, 128 columns
+//   P[g] = 2^(S/8 log2e - m)   TMEM, bf16 pairs, 64 columns
+//   O[g] += P[g] V_j           TMEM, fp32, 64 columns (A operand read from TMEM)
+// and its own running maximum m and sum l per row; a group finishes its tile
+// alone (no merge).  m is a reference maximum in log2 units, raised (and
+// O[g], l rescaled) only when a block's maximum exceeds it by more than 8, so
+// that P <= 2^8.
+// Warp 8 is the TMA producer; warps 9 and 10 issue the MMAs of group 0 and
+// group 1.  One issuing thread per group: a tcgen05.mma takes about 60 cycles
+// to issue from one thread, and the products here are small (N = 128 for S,
+// N = 64 for P V), so one thread issuing for both groups would leave the
+// tensor pipe idle; two threads on two SM sub-partitions issue concurrently
+// (measured on GB300: 45 -> 33 us on B8 S1024 H16).  Warp 11 is spare, so
+// that each issuing warp has an SM sub-partition of its own.
+constexpr int FWD_THREADS = 384;
+constexpr int FWD_NST = 4;                                  // K/V ring stages
+constexpr uint32_t F_S = 0, F_P = 256, F_O = 384;           // TMEM columns of S[0], P[0], O[0]
+constexpr float RESCALE_T = 8.0f;
+
+struct FwdUnit {
+  int h, b;
+  int qlo, qhi;        // query blocks 2p and 2p + 1; qhi < 0: the pair has one block
+};
+
+__device__ __forceinline__ bool fwd_unit(int k, int n_units, int npair, int nqb, int H,
+                                         FwdUnit& U) {
+  const int G = gridDim.x;
+  const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  if (u >= n_units) return false;
+  const int hb = n_units / npair;
+  const int p = npair - 1 - u / hb;
+  U.h = (u % hb) % H;
+  U.b = (u % hb) / H;
+  U.qlo = 2 * p;
+  U.qhi = 2 * p + 1 < nqb ? 2 * p + 1 : -1;
+  return true;
+}
+// query block of group g in the CTA's k-th unit (-1: none) and its tile index
+// in the unit's Q slot
+__device__ __forceinline__ int fwd_grp_q(const FwdUnit& U, int k, int g) {
+  return ((g ^ (k & 1)) == 0) ? U.qlo : U.qhi;
+}
+__device__ __forceinline__ int fwd_grp_t(int k, int g) { return g ^ (k & 1); }
+// K/V blocks a unit loads
+__device__ __forceinline__ int fwd_nkv(const FwdUnit& U) { return (U.qhi >= 0 ? U.qhi : U.qlo) + 1; }
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sQ = sm;                          // [2 slots]
-  uint8_t* sK = sQ + 2 * TILE;               // [FWD_NST]
+  uint8_t* sQ = sm;                          // [2 slots][2 tiles]
+  uint8_t* sK = sQ + 4 * TILE;               // [FWD_NST]
   uint8_t* sV = sK + FWD_NST * TILE;         // [FWD_NST]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sV + FWD_NST * TILE);
   uint64_t *q_full = bar, *q_empty = bar + 2, *kv_full = bar + 4, *kv_empty = kv_full + FWD_NST;
   uint64_t *s_full = kv_empty + FWD_NST, *s_free = s_full + 2, *p_full = s_full + 4,
            *o_done = s_full + 6, *o_free = s_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 24);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* xch = reinterpret_cast<float*>(bar + 32);    // [m, l][2 groups][128]: unit-end merge
   const int nqb = A.S / AB;
-  const int n_units = nqb * A.H * nb;
+  const int npair = (nqb + 1) / 2;
+  const int n_units = npair * A.H * nb;
   const int d = A.H * AD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
+      mbar_init(&q_empty[i], 2);            // both groups' last S of the unit
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], NSWT / 2);     // one softmax group
+      mbar_init(&s_free[i], NSWT / 2);      // one group
       mbar_init(&p_full[i], NSWT / 2);
       mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], NSWT / 2);
     }
-    mbar_init(o_free, NSWT);                // both groups
     for (int i = 0; i < FWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);           // both groups' last P V of the block
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -220,17 +244,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       bool ok = true;
-      int g = 0;
+      int gkv = 0;
       FwdUnit U;
-      for (int k = 0; ok && fwd_unit(k, n_units, nqb, A.H, U); ++k) {
+      for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
         const int row0 = U.b * A.S, slot = k & 1;
         ok = mbar_wait(&q_empty[slot], ((k >> 1) & 1) ^ 1);
         if (!ok) break;
-        mbar_expect_tx(&q_full[slot], TILE);
-        tma_load_2d(sQ + slot * TILE, &tm_qkv, &q_full[slot], U.h * AD, row0 + U.qb * AB);
-        for (int j = 0; j <= U.qb; ++j, ++g) {
-          const int st = g % FWD_NST;
-          ok = mbar_wait(&kv_empty[st], ((g / FWD_NST) & 1) ^ 1);
+        mbar_expect_tx(&q_full[slot], (U.qhi >= 0 ? 2 : 1) * TILE);
+        tma_load_2d(sQ + (2 * slot) * TILE, &tm_qkv, &q_full[slot], U.h * AD, row0 + U.qlo * AB);
+        if (U.qhi >= 0)
+          tma_load_2d(sQ + (2 * slot + 1) * TILE, &tm_qkv, &q_full[slot], U.h * AD,
+                      row0 + U.qhi * AB);
+        const int nkv = fwd_nkv(U);
+        for (int j = 0; j < nkv; ++j, ++gkv) {
+          const int st = gkv % FWD_NST;
+          ok = mbar_wait(&kv_empty[st], ((gkv / FWD_NST) & 1) ^ 1);
           if (!ok) break;
           mbar_expect_tx(&kv_full[st], 2 * TILE);
           tma_load_2d(sK + st * TILE, &tm_qkv, &kv_full[st], d + U.h * AD, row0 + j * AB);
@@ -239,110 +267,119 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- MMA issuer of group g ----------------
     if (lane == 0) {
-      // descriptors of the first tile of each buffer; a tile further is
-      // TILE >> 4 further, a K step 32 bytes (K-major) or 16 rows (V, MN-major)
+      const int g = warp - 9;
       constexpr uint64_t TSTEP = TILE >> 4;
       const uint64_t dq0 = kdesc(sQ, 0), dk0 = kdesc(sK, 0), dv0 = mndesc(sV, 0);
-      // Two cursors walk the same sequence of (unit, key block): one issues
-      // S = Q K^T as soon as the block's K/V and S buffer are ready, the
-      // other P V as soon as the block's P is; neither waits on the other's
-      // barriers, so the tensor core gets whichever product is ready first.
-      struct Cursor {
-        int k, j, g;
+      // A cursor walks this group's items (unit k, key block j) in order:
+      // base is the ring index of the unit's first K/V block, c the group's
+      // item count, e its count of units with work.
+      struct Cur {
+        int k, j, n, base, c, e;
         FwdUnit U;
         bool valid;
       };
-      auto advance = [&](Cursor& c) {
-        ++c.g;
-        if (++c.j > c.U.qb) {
-          c.j = 0;
+      auto enter = [&](Cur& c) {   // the group's next unit with work
+        while ((c.valid = fwd_unit(c.k, n_units, npair, nqb, A.H, c.U))) {
+          const int q = fwd_grp_q(c.U, c.k, g);
+          if (q >= 0) {
+            c.n = q + 1;
+            return;
+          }
+          c.base += fwd_nkv(c.U);
           ++c.k;
-          c.valid = fwd_unit(c.k, n_units, nqb, A.H, c.U);
         }
       };
-      Cursor cq, cp;
-      cq.k = cq.j = cq.g = 0;
-      cq.valid = fwd_unit(0, n_units, nqb, A.H, cq.U);
-      cp = cq;
+      auto next = [&](Cur& c) {
+        ++c.c;
+        if (++c.j >= c.n) {
+          c.base += fwd_nkv(c.U);
+          c.j = 0;
+          ++c.k;
+          ++c.e;
+          enter(c);
+        }
+      };
+      Cur cs, cp;
+      cs.k = cs.j = cs.base = cs.c = cs.e = 0;
+      enter(cs);
+      cp = cs;
+      // The group's products come in a fixed order -- S of item c + 1 (once
+      // the softmax has read S of item c) before P V of item c (once it has
+      // written P of item c) -- so the issuer waits for each in turn.
+      auto issue_s = [&]() -> bool {
+        const int gkv = cs.base + cs.j, st = gkv % FWD_NST, slot = cs.k & 1;
+        if (cs.j == 0 && !mbar_wait(&q_full[slot], (cs.k >> 1) & 1)) return false;
+        if (!mbar_wait(&kv_full[st], (gkv / FWD_NST) & 1)) return false;
+        if (cs.c > 0 && !mbar_wait(&s_free[g], (cs.c - 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t aq = dq0 + (uint64_t)(2 * slot + fwd_grp_t(cs.k, g)) * TSTEP;
+        const uint64_t bk = dk0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AD / 16; ++kk)
+          mma_bf16(tbase + F_S + 128 * g, aq + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
+        mma_commit(&s_full[g]);
+        if (cs.j == cs.n - 1) {
+          mma_commit(&q_empty[slot]);
+          if (cs.U.qhi < 0) mma_commit(&q_empty[slot]);   // the other group had no block
+        }
+        next(cs);
+        return true;
+      };
+      auto issue_pv = [&]() -> bool {
+        if (!mbar_wait(&p_full[g], cp.c & 1)) return false;
+        // a unit's first P V overwrites O[g]: the previous unit's O is read out
+        if (cp.j == 0 && cp.e > 0 && !mbar_wait(&o_free[g], (cp.e - 1) & 1)) return false;
+        tc_fence_after();
+        const int st = (cp.base + cp.j) % FWD_NST;
+        const uint64_t bv = dv0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AB / 16; ++kk)
+          mma_bf16_ts(tbase + F_O + 64 * g, tbase + F_P + 64 * g + kk * 8, bv + kk * 128,
+                      IDESC_128x64_KMN, kk > 0 || cp.j > 0);
+        mma_commit(&o_done[g]);
+        mma_commit(&kv_empty[st]);
+        // the other group does not use this key block: its arrival too
+        const int qo = fwd_grp_q(cp.U, cp.k, g ^ 1);
+        if (qo < 0 || cp.j > qo) mma_commit(&kv_empty[st]);
+        next(cp);
+        return true;
+      };
       bool ok = true;
-      uint32_t idle = 0;
-      while (cp.valid) {
-        bool did = false;
-        if (cq.valid) {
-          const int st = cq.g % FWD_NST, sb = cq.g & 1, slot = cq.k & 1;
-          // S[sb] was last read by its group two blocks ago
-          if ((cq.j > 0 || mbar_test(&q_full[slot], (cq.k >> 1) & 1)) &&
-              mbar_test(&kv_full[st], (cq.g / FWD_NST) & 1) &&
-              (cq.g < 2 || mbar_test(&s_free[sb], ((cq.g - 2) >> 1) & 1))) {
-            tc_fence_after();
-            const uint64_t aq = dq0 + (uint64_t)slot * TSTEP;
-            const uint64_t bk = dk0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AD / 16; ++kk)
-              mma_bf16(tbase + F_S + 128 * sb, aq + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
-            mma_commit(&s_full[sb]);
-            if (cq.j == cq.U.qb) mma_commit(&q_empty[slot]);
-            advance(cq);
-            did = true;
-          }
-        }
-        if (cp.g < cq.g) {
-          const int pb = cp.g & 1;
-          // a unit's first product overwrites O: the previous unit's O is read out
-          if (mbar_test(&p_full[pb], (cp.g >> 1) & 1) &&
-              (cp.j != 0 || cp.k == 0 || mbar_test(o_free, (cp.k - 1) & 1))) {
-            tc_fence_after();
-            const int st = cp.g % FWD_NST;
-            const uint64_t bv = dv0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AB / 16; ++kk)
-              mma_bf16_ts(tbase + F_O + 64 * pb, tbase + F_P + 64 * pb + kk * 8, bv + kk * 128,
-                          IDESC_128x64_KMN, kk > 0 || cp.j >= 2);
-            mma_commit(&o_done[pb]);
-            mma_commit(&kv_empty[st]);
-            advance(cp);
-            did = true;
-          }
-        }
-        if (did) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          ok = false;
-          break;
-        }
+      if (cs.valid) ok = issue_s();
+      while (ok && cp.valid) {
+        if (cs.valid) ok = issue_s();
+        if (ok) ok = issue_pv();
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else {
-    // ---------------- softmax: two groups of four warps ----------------
+  } else if (warp < 8) {
+    // ---------------- softmax: group g = warps 4g .. 4g+3, one row per thread ----------------
     const int quarter = warp & 3;
-    const int grp = warp >> 2;
+    const int g = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tbase + F_S + 128 * grp + lane_off;
-    const uint32_t tP = tbase + F_P + 64 * grp + lane_off;
-    const uint32_t tO = tbase + F_O + 64 * grp + lane_off;
-    const float scale2 = LOG2E * 0.125f;      // log2(e) / sqrt(64)
+    const uint32_t tS = tbase + F_S + 128 * g + lane_off;
+    const uint32_t tP = tbase + F_P + 64 * g + lane_off;
+    const uint32_t tO = tbase + F_O + 64 * g + lane_off;
+    const float scale2 = LOG2E * 0.125f;
     bool ok = true;
-    int g0 = 0;                               // running index of the unit's first block
+    int c = 0;   // this group's item count
     FwdUnit U;
-    // Both groups pass the unit-end barrier, also after a failed wait, so
-    // that a timeout never leaves the partner warp blocked there.
-    for (int k = 0; fwd_unit(k, n_units, nqb, A.H, U); ++k) {
-      const int n = U.qb + 1;
+    for (int k = 0; ok && fwd_unit(k, n_units, npair, nqb, A.H, U); ++k) {
+      const int q = fwd_grp_q(U, k, g);
+      if (q < 0) continue;
+      const int n = q + 1;
       float m = -INFINITY, l = 0.0f;
-      int last = -1;                          // running index of this group's last block
-      for (int j = (grp - g0) & 1; ok && j < n; j += 2) {
-        const int gi = g0 + j;
-        if (!mbar_wait(&s_full[grp], (gi >> 1) & 1)) {
+      for (int j = 0; j < n; ++j, ++c) {
+        if (!mbar_wait(&s_full[g], c & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // the whole 128-column row of S in registers, then S[grp] is released
+        // the whole 128-column row of S in registers, then S[g] is released
         uint32_t sv[4][32];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) tmem_ld32_async(tS + 32 * ch, sv[ch]);
@@ -351,45 +388,88 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         reg_fence(sv[2]);
         reg_fence(sv[3]);
         tc_fence_before();
-        mbar_arrive(&s_free[grp]);
-        if (j == U.qb) {
+        mbar_arrive(&s_free[g]);
+        // the diagonal block: 32-key chunk `quarter` holds this warp's
+        // diagonal (keys after the row masked), later chunks are masked whole
+        const bool diag = (j == n - 1);
+        const int lim = diag ? quarter : 3;   // last chunk with an unmasked key
+        if (diag) {
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) mask_diag(sv[ch], 32 * ch, r);
+          for (int ch = 0; ch < 4; ++ch)
+            if (ch == quarter) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e > lane) sv[ch][e] = 0xff800000u;
+            }
         }
-        float pm[8];
+        float pm[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) pm[e] = __uint_as_float(sv[0][e]);
+        for (int ch = 0; ch < 4; ++ch) {
+          pm[ch] = -INFINITY;
+          if (ch <= lim) {
+            // tree of three-input maxima: 32 -> 11 -> 4 -> 1
+            float t1[11];
 #pragma unroll
-        for (int e = 8; e < 128; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
-        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale2;
+            for (int i = 0; i < 10; ++i)
+              t1[i] = max3f(__uint_as_float(sv[ch][3 * i]), __uint_as_float(sv[ch][3 * i + 1]),
+                            __uint_as_float(sv[ch][3 * i + 2]));
+            t1[10] = fmaxf(__uint_as_float(sv[ch][30]), __uint_as_float(sv[ch][31]));
+            const float t2a = max3f(t1[0], t1[1], t1[2]), t2b = max3f(t1[3], t1[4], t1[5]),
+                        t2c = max3f(t1[6], t1[7], t1[8]), t2d = fmaxf(t1[9], t1[10]);
+            pm[ch] = fmaxf(max3f(t2a, t2b, t2c), t2d);
+          }
+        }
+        const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale2;
         const bool need = mx > m + RESCALE_T;
         const float m_new = need ? mx : m;
         const float alpha = need ? exp2f(m - m_new) : 1.0f;
-        // P[grp] and O[grp] are free once this group's previous P V is done
-        if (gi >= 2 && !mbar_wait(&o_done[grp], ((gi - 2) >> 1) & 1)) {
+        const float2 sc2 = make_float2(scale2, scale2), nm2 = make_float2(-m_new, -m_new);
+        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        // chunks 0-1 while the previous P V may still read P[g]; then wait for
+        // it, store them and go on with chunks 2-3; masked chunks store zeros
+        uint32_t pk[2][16];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          if (ch <= lim) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 y = __ffma2_rn(u2f2(sv[ch][e], sv[ch][e + 1]), sc2, nm2);
+              const float2 pe = make_float2(ex2(y.x), ex2(y.y));
+              ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], pe);
+              pk[ch][e >> 1] = pack_bf16(pe.x, pe.y);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[ch][e] = 0u;
+          }
+        }
+        // P[g] and O[g] are free once this group's previous P V is done
+        if (c >= 1 && !mbar_wait(&o_done[g], (c - 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float2 sc2 = make_float2(scale2, scale2), nm2 = make_float2(-m_new, -m_new);
-        float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        tmem_st16(tP, pk[0]);
+        tmem_st16(tP + 16, pk[1]);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
+        for (int ch = 2; ch < 4; ++ch) {
+          uint32_t pq[16];
+          if (ch <= lim) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 y = __ffma2_rn(u2f2(sv[ch][e], sv[ch][e + 1]), sc2, nm2);
-            // one pair in four on the FMA pipe, the rest on the SFU
-            const float2 pe = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
-            ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], pe);
-            __nv_bfloat162 hv = __floats2bfloat162_rn(pe.x, pe.y);
-            pk[e >> 1] = *reinterpret_cast<uint32_t*>(&hv);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 y = __ffma2_rn(u2f2(sv[ch][e], sv[ch][e + 1]), sc2, nm2);
+              const float2 pe = make_float2(ex2(y.x), ex2(y.y));
+              ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], pe);
+              pq[e >> 1] = pack_bf16(pe.x, pe.y);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pq[e] = 0u;
           }
-          tmem_st16(tP + 16 * ch, pk);
+          tmem_st16(tP + 16 * ch, pq);
         }
-        // O[grp] = O[grp] * alpha for the rows whose reference maximum moved
-        if (last >= 0 && __any_sync(0xffffffffu, need)) {
+        // O[g] = O[g] * alpha for the rows whose reference maximum moved
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -408,49 +488,32 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&p_full[grp]);
+        mbar_arrive(&p_full[g]);
         const float2 lsp = __fadd2_rn(ls[0], ls[1]);
         l = l * alpha + (lsp.x + lsp.y);
         m = m_new;
-        last = gi;
       }
-      // unit end: this group's O is complete once its last P V is done
-      if (ok && last >= 0) ok = mbar_wait(&o_done[grp], (last >> 1) & 1);
-      xch[grp * AB + r] = m;
-      xch[(2 + grp) * AB + r] = l;
-      tc_fence_before();
-      pair_sync(quarter);
-      if (ok) {
-        tc_fence_after();
-        // group p had blocks in this unit unless the unit's only block went to the other
-        const bool has0 = n >= 2 || (g0 & 1) == 0, has1 = n >= 2 || (g0 & 1) == 1;
-        const float m0 = xch[r], m1 = xch[AB + r];
-        const float M = fmaxf(has0 ? m0 : -INFINITY, has1 ? m1 : -INFINITY);
-        const float w0 = has0 ? exp2f(m0 - M) : 0.0f, w1 = has1 ? exp2f(m1 - M) : 0.0f;
-        const float L = (has0 ? xch[2 * AB + r] * w0 : 0.0f) + (has1 ? xch[3 * AB + r] * w1 : 0.0f);
-        // this thread writes head dimensions 32 grp .. +31 of its row
-        float o[32];
+      if (!ok) break;
+      // unit end: O of this group's tile once its last P V is done
+      if (!mbar_wait(&o_done[g], (c - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int qi = q * AB + r;
+      bf16* orow = A.o + (size_t)(U.b * A.S + qi) * d + U.h * AD;
+      const float inv_l = 1.0f / l;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.0f;
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          if (!(p2 ? has1 : has0)) continue;
-          float ov[32];
-          tmem_ld32(tbase + F_O + 64 * p2 + 32 * grp + lane_off, ov);
-          const float wp = p2 ? w1 : w0;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = fmaf(ov[e], wp, o[e]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float ov[32];
+        tmem_ld32(tO + 32 * hh, ov);
+        if (hh == 1) {
+          tc_fence_before();
+          mbar_arrive(&o_free[g]);            // O[g] is read: the next unit may overwrite it
         }
-        const int qi = U.qb * AB + r;
-        store8_bf16_row(A.o + (size_t)(U.b * A.S + qi) * d + U.h * AD + 32 * grp, o, 1.0f / L);
-        if (grp == 0) A.lse[((size_t)U.b * A.H + U.h) * A.S + qi] = (M + log2f(L)) / LOG2E;
-        tc_fence_before();
+        store8_bf16_row(orow + 32 * hh, ov, inv_l);
       }
-      // xch is rewritten at the next unit's end only after both warps passed
-      // this point (the next pair_sync orders it)
-      pair_sync(quarter);
-      mbar_arrive(o_free);
-      g0 += n;
+      A.lse[((size_t)U.b * A.H + U.h) * A.S + qi] = (m + log2f(l)) / LOG2E;
     }
     if (!ok) fail_wait(A.err, abort_flag);
   }
@@ -470,7 +533,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // elementwise work (warp w: TMEM lane quarter w & 3, columns 64 (w >> 2) ..
 // +63), S and dP read from TMEM once and released, and the bf16 products P /
 // dS written back into TMEM as the A operand of the accumulating MMAs.
-constexpr int BWD_THREADS = 320;
+constexpr int BWD_THREADS = 384;   // warps 0-7 elementwise, 8 TMA, 9-10 MMA, 11 spare
 constexpr int BWD_NST = 3;   // ring stages of the streamed operand pair
 
 __device__ __forceinline__ bool bwd_unit(int k, int n_units, int hb, int H, int& major, int& h,
@@ -506,10 +569,6 @@ __device__ __forceinline__ void tmem_ld4x32(uint32_t t0, uint32_t t1, uint32_t t
   reg_fence(e);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
-  __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
-  return *reinterpret_cast<uint32_t*>(&hv);
-}
 
 // ------------------------------------------------------------ dK / dV
 // Unit: key block jb; over the query blocks i = jb .. nqb-1 (keys are the M
@@ -545,18 +604,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // barriers the MMAs complete take one commit from each of the two issuers
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);
     }
     for (int i = 0; i < BWD_NST; ++i) {
       mbar_init(&in_full[i], 1);
-      mbar_init(&in_empty[i], 1);
+      mbar_init(&in_empty[i], 2);
     }
-    mbar_init(st_full, 1);
+    mbar_init(st_full, 2);
     mbar_init(st_free, NSWT);
     mbar_init(ds_full, NSWT);
-    mbar_init(acc_done, 1);
+    mbar_init(acc_done, 2);
     mbar_init(o_free, NSWT);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -593,12 +653,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- MMA issuers ----------------
+    // Issuer 0 (warp 9): S^T = K Q_i^T, then dV += P^T dO_i; issuer 1 (warp
+    // 10): dP^T = V dO_i^T, then dK += dS^T Q_i.  Twelve MMAs each per block;
+    // two issuing threads on two SM sub-partitions keep the tensor pipe fed
+    // where one thread issuing all 24 small MMAs could not.  Each issues, in
+    // order, its S-type product of block c + 1 (once the elementwise warps have
+    // read block c's S^T and dP^T) before its accumulating product of block c
+    // (once they have written P^T and dS^T of block c).
     if (lane == 0) {
+      const int who = warp - 9;
       constexpr uint64_t TSTEP = TILE >> 4;
-      const uint64_t dk0 = kdesc(sK, 0), dv0 = kdesc(sV, 0), dq0 = kdesc(sQ, 0),
-                     ddo0 = kdesc(sdO, 0), mq0 = mndesc(sQ, 0), mdo0 = mndesc(sdO, 0);
+      const uint64_t da0 = who == 0 ? kdesc(sK, 0) : kdesc(sV, 0);        // K or V
+      const uint64_t db0 = who == 0 ? kdesc(sQ, 0) : kdesc(sdO, 0);       // Q_i or dO_i
+      const uint64_t dm0 = who == 0 ? mndesc(sdO, 0) : mndesc(sQ, 0);     // dO_i or Q_i
+      const uint32_t t_st = tbase + (who == 0 ? DKV_S : DKV_DP);
+      const uint32_t t_a = tbase + (who == 0 ? DKV_P : DKV_DS);
+      const uint32_t t_acc = tbase + (who == 0 ? DKV_DV : DKV_DK);
       struct Cursor {
         int k, j, g, jb, h, b;
         bool valid;
@@ -615,61 +687,47 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ca.k = ca.j = ca.g = 0;
       ca.valid = bwd_unit(0, n_units, hb, A.H, ca.jb, ca.h, ca.b);
       Cursor cb = ca;
+      auto issue_st = [&]() -> bool {
+        const int st = ca.g % BWD_NST, slot = ca.k & 1;
+        if (ca.j == 0 && !mbar_wait(&kv_full[slot], (ca.k >> 1) & 1)) return false;
+        if (!mbar_wait(&in_full[st], (ca.g / BWD_NST) & 1)) return false;
+        if (ca.g > 0 && !mbar_wait(st_free, (ca.g - 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t a = da0 + (uint64_t)slot * TSTEP, bq = db0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AD / 16; ++kk)
+          mma_bf16(t_st, a + kk * 2, bq + kk * 2, IDESC_128x128_KK, kk > 0);
+        mma_commit(st_full);
+        if (ca.j == nqb - ca.jb - 1) mma_commit(&kv_empty[slot]);
+        advance(ca);
+        return true;
+      };
+      auto issue_acc = [&]() -> bool {
+        if (!mbar_wait(ds_full, cb.g & 1)) return false;
+        // a unit's first block overwrites the accumulator: the previous
+        // unit's dV / dK is read out
+        if (cb.j == 0 && cb.k > 0 && !mbar_wait(o_free, (cb.k - 1) & 1)) return false;
+        tc_fence_after();
+        const int st = cb.g % BWD_NST;
+        const uint64_t bm = dm0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AB / 16; ++kk)
+          mma_bf16_ts(t_acc, t_a + kk * 8, bm + kk * 128, IDESC_128x64_KMN, kk > 0 || cb.j > 0);
+        mma_commit(acc_done);
+        mma_commit(&in_empty[st]);
+        advance(cb);
+        return true;
+      };
       bool ok = true;
-      uint32_t idle = 0;
-      while (cb.valid) {
-        bool did = false;
-        if (ca.valid) {
-          const int st = ca.g % BWD_NST, slot = ca.k & 1;
-          if ((ca.j > 0 || mbar_test(&kv_full[slot], (ca.k >> 1) & 1)) &&
-              mbar_test(&in_full[st], (ca.g / BWD_NST) & 1) &&
-              (ca.g == 0 || mbar_test(st_free, (ca.g - 1) & 1))) {
-            tc_fence_after();
-            const uint64_t ak = dk0 + (uint64_t)slot * TSTEP, av = dv0 + (uint64_t)slot * TSTEP;
-            const uint64_t bq = dq0 + (uint64_t)st * TSTEP, bo = ddo0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AD / 16; ++kk)
-              mma_bf16(tbase + DKV_S, ak + kk * 2, bq + kk * 2, IDESC_128x128_KK, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < AD / 16; ++kk)
-              mma_bf16(tbase + DKV_DP, av + kk * 2, bo + kk * 2, IDESC_128x128_KK, kk > 0);
-            mma_commit(st_full);
-            if (ca.j == nqb - ca.jb - 1) mma_commit(&kv_empty[slot]);
-            advance(ca);
-            did = true;
-          }
-        }
-        if (cb.g < ca.g) {
-          // dV and dK overwrite their accumulators at a unit's first block:
-          // the previous unit's results are read out
-          if (mbar_test(ds_full, cb.g & 1) &&
-              (cb.j != 0 || cb.k == 0 || mbar_test(o_free, (cb.k - 1) & 1))) {
-            tc_fence_after();
-            const int st = cb.g % BWD_NST;
-            const uint64_t bo = mdo0 + (uint64_t)st * TSTEP, bq = mq0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AB / 16; ++kk)
-              mma_bf16_ts(tbase + DKV_DV, tbase + DKV_P + kk * 8, bo + kk * 128, IDESC_128x64_KMN,
-                          kk > 0 || cb.j > 0);
-#pragma unroll
-            for (int kk = 0; kk < AB / 16; ++kk)
-              mma_bf16_ts(tbase + DKV_DK, tbase + DKV_DS + kk * 8, bq + kk * 128, IDESC_128x64_KMN,
-                          kk > 0 || cb.j > 0);
-            mma_commit(acc_done);
-            mma_commit(&in_empty[st]);
-            advance(cb);
-            did = true;
-          }
-        }
-        if (did) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          ok = false;
-          break;
-        }
+      if (ca.valid) ok = issue_st();
+      while (ok && cb.valid) {
+        if (ca.valid) ok = issue_st();
+        if (ok) ok = issue_acc();
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
+  } else if (warp == 11) {
+    // spare warp: each issuing warp keeps an SM sub-partition of its own
   } else {
     // ---------------- elementwise: warps 0-7 ----------------
     const int quarter = warp & 3;
@@ -795,17 +853,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // barriers that both issuers' MMAs complete take one commit from each
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qd_full[i], 1);
-      mbar_init(&qd_empty[i], 1);
+      mbar_init(&qd_empty[i], 2);
       mbar_init(&ds_full[i], NSWT);
       mbar_init(&dq_done[i], 1);
     }
     for (int i = 0; i < BWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);
     }
-    mbar_init(s_full, 1);
+    mbar_init(s_full, 2);
     mbar_init(s_free, NSWT);
     mbar_init(o_free, NSWT);
     *abort_flag = 0;
@@ -840,12 +899,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- MMA issuers ----------------
+    // Issuer 0 (warp 9): S = Q K_j^T, then dQ += dS K_j; issuer 1 (warp 10):
+    // dP = dO V_j^T.  Issuer 0 issues S of block c + 1 (once the elementwise
+    // warps have read block c's S and dP) before dQ of block c (once they have
+    // written dS of block c).
     if (lane == 0) {
+      const int who = warp - 9;
       constexpr uint64_t TSTEP = TILE >> 4;
-      const uint64_t dq0 = kdesc(sQ, 0), ddo0 = kdesc(sdO, 0), dk0 = kdesc(sK, 0),
-                     dv0 = kdesc(sV, 0), mk0 = mndesc(sK, 0);
+      const uint64_t da0 = who == 0 ? kdesc(sQ, 0) : kdesc(sdO, 0);   // Q or dO
+      const uint64_t db0 = who == 0 ? kdesc(sK, 0) : kdesc(sV, 0);    // K_j or V_j
+      const uint64_t mk0 = mndesc(sK, 0);
+      const uint32_t t_st = tbase + (who == 0 ? DQ_S : DQ_DP);
       struct Cursor {
         int k, j, g, ib, h, b;
         bool valid;
@@ -867,57 +933,53 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ca.k = ca.j = ca.g = 0;
       load_unit(ca);
       Cursor cb = ca;
+      auto issue_st = [&]() -> bool {
+        const int st = ca.g % BWD_NST, slot = ca.k & 1;
+        if (ca.j == 0 && !mbar_wait(&qd_full[slot], (ca.k >> 1) & 1)) return false;
+        if (!mbar_wait(&kv_full[st], (ca.g / BWD_NST) & 1)) return false;
+        if (ca.g > 0 && !mbar_wait(s_free, (ca.g - 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t a = da0 + (uint64_t)slot * TSTEP, bk = db0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AD / 16; ++kk)
+          mma_bf16(t_st, a + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
+        mma_commit(s_full);
+        if (ca.j == ca.ib) mma_commit(&qd_empty[slot]);
+        if (who == 1) mma_commit(&kv_empty[st]);   // V_j is done with once dP is
+        advance(ca);
+        return true;
+      };
+      auto issue_dq = [&]() -> bool {
+        const int pb = cb.g & 1;
+        if (!mbar_wait(&ds_full[pb], (cb.g >> 1) & 1)) return false;
+        // dQ is overwritten at a unit's first block: the previous unit's dQ is read out
+        if (cb.j == 0 && cb.k > 0 && !mbar_wait(o_free, (cb.k - 1) & 1)) return false;
+        tc_fence_after();
+        const int st = cb.g % BWD_NST;
+        const uint64_t bk = mk0 + (uint64_t)st * TSTEP;
+#pragma unroll
+        for (int kk = 0; kk < AB / 16; ++kk)
+          mma_bf16_ts(tbase + DQ_DQ, tbase + DQ_DS + 64 * pb + kk * 8, bk + kk * 128,
+                      IDESC_128x64_KMN, kk > 0 || cb.j > 0);
+        mma_commit(&dq_done[pb]);
+        mma_commit(&kv_empty[st]);                 // K_j (S and dQ) is done with
+        advance(cb);
+        return true;
+      };
       bool ok = true;
-      uint32_t idle = 0;
-      while (cb.valid) {
-        bool did = false;
-        if (ca.valid) {
-          const int st = ca.g % BWD_NST, slot = ca.k & 1;
-          if ((ca.j > 0 || mbar_test(&qd_full[slot], (ca.k >> 1) & 1)) &&
-              mbar_test(&kv_full[st], (ca.g / BWD_NST) & 1) &&
-              (ca.g == 0 || mbar_test(s_free, (ca.g - 1) & 1))) {
-            tc_fence_after();
-            const uint64_t aq = dq0 + (uint64_t)slot * TSTEP, ao = ddo0 + (uint64_t)slot * TSTEP;
-            const uint64_t bk = dk0 + (uint64_t)st * TSTEP, bv = dv0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AD / 16; ++kk)
-              mma_bf16(tbase + DQ_S, aq + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < AD / 16; ++kk)
-              mma_bf16(tbase + DQ_DP, ao + kk * 2, bv + kk * 2, IDESC_128x128_KK, kk > 0);
-            mma_commit(s_full);
-            if (ca.j == ca.ib) mma_commit(&qd_empty[slot]);
-            advance(ca);
-            did = true;
-          }
-        }
-        if (cb.g < ca.g) {
-          const int pb = cb.g & 1;
-          // dQ is overwritten at a unit's first block: the previous unit's dQ is read out
-          if (mbar_test(&ds_full[pb], (cb.g >> 1) & 1) &&
-              (cb.j != 0 || cb.k == 0 || mbar_test(o_free, (cb.k - 1) & 1))) {
-            tc_fence_after();
-            const int st = cb.g % BWD_NST;
-            const uint64_t bk = mk0 + (uint64_t)st * TSTEP;
-#pragma unroll
-            for (int kk = 0; kk < AB / 16; ++kk)
-              mma_bf16_ts(tbase + DQ_DQ, tbase + DQ_DS + 64 * pb + kk * 8, bk + kk * 128,
-                          IDESC_128x64_KMN, kk > 0 || cb.j > 0);
-            mma_commit(&dq_done[pb]);
-            mma_commit(&kv_empty[st]);
-            advance(cb);
-            did = true;
-          }
-        }
-        if (did) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          ok = false;
-          break;
+      if (who == 1) {
+        while (ok && ca.valid) ok = issue_st();
+      } else {
+        if (ca.valid) ok = issue_st();
+        while (ok && cb.valid) {
+          if (ca.valid) ok = issue_st();
+          if (ok) ok = issue_dq();
         }
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
+  } else if (warp == 11) {
+    // spare warp: each issuing warp keeps an SM sub-partition of its own
   } else {
     // ---------------- elementwise: warps 0-7 ----------------
     const int quarter = warp & 3;
@@ -1032,7 +1094,7 @@ bool map_128x64(CUtensorMap* m, const void* base, long long rows, long long cols
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t SMEM_FWD = 1024 + TILE * (2 + 2 * FWD_NST) + 256 + 4 * AB * 4;
+constexpr size_t SMEM_FWD = 1024 + TILE * (4 + 2 * FWD_NST) + 256;
 constexpr size_t SMEM_DKDV = 1024 + TILE * (4 + 2 * BWD_NST) + 2 * BWD_NST * AB * 4 + 256;
 constexpr size_t SMEM_DQ = 1024 + TILE * (4 + 2 * BWD_NST) + 256;
 
@@ -1062,7 +1124,7 @@ cudaError_t attn_fwd_tc_launch(const void* qkv, void* o, float* lse, int nb, int
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int units = (S / AB) * H * nb;
+  const int units = ((S / AB + 1) / 2) * H * nb;
   attn_fwd_tc<<<units < sms ? units : sms, FWD_THREADS, SMEM_FWD, s>>>(m, a, nb);
   return cudaGetLastError();
 }
