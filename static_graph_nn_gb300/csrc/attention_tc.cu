@@ -577,9 +577,44 @@ __device__ __forceinline__ void tmem_ld4x32(uint32_t t0, uint32_t t1, uint32_t t
 //   P^T = 2^(S^T/8 log2e - LSE_i log2e), dS^T = P^T (dP^T - D_i)  -> TMEM bf16
 //   dV += P^T dO_i, dK += dS^T Q_i                      TMEM, fp32
 // dK is scaled by 1/8 when it is written out.
+// Warps 0-15 do the elementwise work, four per TMEM lane quarter: warp w
+// takes key rows 32 (w & 3) .. +31 and query columns 32 (w >> 2) .. +31, so
+// that each SM sub-partition has four elementwise warps to hide the latency
+// of the per-element chain (TMEM load, exp2, products, bf16 packing, TMEM
+// store).  Warp 16 is the TMA producer; warps 17 and 18 issue the MMAs.
 constexpr uint32_t DKV_S = 0, DKV_DP = 128, DKV_P = 256, DKV_DS = 320, DKV_DV = 384, DKV_DK = 448;
+constexpr int DKV_THREADS = 608;
+constexpr int DKV_EW = 512;                 // elementwise threads
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 fp32 values times scale -> bf16, two 16-byte global stores.
+__device__ __forceinline__ void store16_bf16(bf16* out, const float* v, float scale) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint4 u;
+    u.x = pack_bf16(v[q * 8 + 0] * scale, v[q * 8 + 1] * scale);
+    u.y = pack_bf16(v[q * 8 + 2] * scale, v[q * 8 + 3] * scale);
+    u.z = pack_bf16(v[q * 8 + 4] * scale, v[q * 8 + 5] * scale);
+    u.w = pack_bf16(v[q * 8 + 6] * scale, v[q * 8 + 7] * scale);
+    reinterpret_cast<uint4*>(out)[q] = u;
+  }
+}
+
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tm_qkv,
                      const __grid_constant__ CUtensorMap tm_do, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
@@ -614,20 +649,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(&in_empty[i], 2);
     }
     mbar_init(st_full, 2);
-    mbar_init(st_free, NSWT);
-    mbar_init(ds_full, NSWT);
+    mbar_init(st_free, DKV_EW);
+    mbar_init(ds_full, DKV_EW);
     mbar_init(acc_done, 2);
-    mbar_init(o_free, NSWT);
+    mbar_init(o_free, DKV_EW);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) tmem_alloc(tmem_slot, 512);
+  if (warp == 16) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 16) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       bool ok = true;
@@ -653,17 +688,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp == 17 || warp == 18) {
     // ---------------- MMA issuers ----------------
-    // Issuer 0 (warp 9): S^T = K Q_i^T, then dV += P^T dO_i; issuer 1 (warp
-    // 10): dP^T = V dO_i^T, then dK += dS^T Q_i.  Twelve MMAs each per block;
+    // Issuer 0 (warp 17): S^T = K Q_i^T, then dV += P^T dO_i; issuer 1 (warp
+    // 18): dP^T = V dO_i^T, then dK += dS^T Q_i.  Twelve MMAs each per block;
     // two issuing threads on two SM sub-partitions keep the tensor pipe fed
     // where one thread issuing all 24 small MMAs could not.  Each issues, in
     // order, its S-type product of block c + 1 (once the elementwise warps have
     // read block c's S^T and dP^T) before its accumulating product of block c
     // (once they have written P^T and dS^T of block c).
     if (lane == 0) {
-      const int who = warp - 9;
+      const int who = warp - 17;
       constexpr uint64_t TSTEP = TILE >> 4;
       const uint64_t da0 = who == 0 ? kdesc(sK, 0) : kdesc(sV, 0);        // K or V
       const uint64_t db0 = who == 0 ? kdesc(sQ, 0) : kdesc(sdO, 0);       // Q_i or dO_i
@@ -726,20 +761,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 11) {
-    // spare warp: each issuing warp keeps an SM sub-partition of its own
-  } else {
-    // ---------------- elementwise: warps 0-7 ----------------
+  } else if (warp < 16) {
+    // ---------------- elementwise: warps 0-15 ----------------
     const int quarter = warp & 3;
-    const int half = warp >> 2;
+    const int part = warp >> 2;                    // query columns 32 part .. +31
     const int r = quarter * 32 + lane;             // key row within the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tbase + DKV_S + 64 * half + lane_off;
-    const uint32_t tDP = tbase + DKV_DP + 64 * half + lane_off;
-    const uint32_t tP = tbase + DKV_P + 32 * half + lane_off;
-    const uint32_t tDS = tbase + DKV_DS + 32 * half + lane_off;
+    const uint32_t tS = tbase + DKV_S + 32 * part + lane_off;
+    const uint32_t tDP = tbase + DKV_DP + 32 * part + lane_off;
+    const uint32_t tP = tbase + DKV_P + 16 * part + lane_off;
+    const uint32_t tDS = tbase + DKV_DS + 16 * part + lane_off;
     const float scale2 = LOG2E * 0.125f;
-    const float2 sc2 = make_float2(scale2, scale2), nlog2 = make_float2(-LOG2E, -LOG2E);
+    const float2 sc2 = make_float2(scale2, scale2);
     bool ok = true;
     int g = 0, jb, h, b;
     for (int k = 0; ok && bwd_unit(k, n_units, hb, A.H, jb, h, b); ++k) {
@@ -751,34 +784,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sv[2][32], dv[2][32];
-        tmem_ld4x32(tS, tS + 32, tDP, tDP + 32, sv[0], sv[1], dv[0], dv[1]);
+        uint32_t sv[32], dv[32];
+        tmem_ld32_async(tS, sv);
+        tmem_ld32_async(tDP, dv);
+        tmem_wait_regs(sv);
+        reg_fence(dv);
         tc_fence_before();
         mbar_arrive(st_free);                      // S^T, dP^T may be overwritten
-        if (j == 0) {
-          mask_diag_t(sv[0], 64 * half, r);
-          mask_diag_t(sv[1], 64 * half + 32, r);
-        }
-        const float* L = sL + st * AB + 64 * half;
-        const float* Dv = sD + st * AB + 64 * half;
-        uint32_t pp[2][16], pd[2][16];
+        if (j == 0) mask_diag_t(sv, 32 * part, r);
+        const float* L = sL + st * AB + 32 * part;
+        const float* Dv = sD + st * AB + 32 * part;
+        uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = reinterpret_cast<const float4*>(L)[e4];
+          const float4 d4 = reinterpret_cast<const float4*>(Dv)[e4];
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = reinterpret_cast<const float4*>(L + 32 * c)[e4];
-            const float4 d4 = reinterpret_cast<const float4*>(Dv + 32 * c)[e4];
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              const int e = e4 * 4 + u;
-              const float2 l2 = u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
-              const float2 d2 = u ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-              const float2 y = __ffma2_rn(u2f2(sv[c][e], sv[c][e + 1]), sc2, __fmul2_rn(l2, nlog2));
-              const float2 p = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
-              const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[c][e], dv[c][e + 1]), d2));
-              pp[c][e >> 1] = pack_bf16(p.x, p.y);
-              pd[c][e >> 1] = pack_bf16(ds.x, ds.y);
-            }
+          for (int u = 0; u < 4; u += 2) {
+            const int e = e4 * 4 + u;
+            const float2 nl = u ? make_float2(-l4.z * LOG2E, -l4.w * LOG2E)
+                                : make_float2(-l4.x * LOG2E, -l4.y * LOG2E);
+            const float2 nd = u ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            const float2 y = __ffma2_rn(u2f2(sv[e], sv[e + 1]), sc2, nl);
+            const float2 p = make_float2(ex2(y.x), ex2(y.y));
+            const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[e], dv[e + 1]), nd));
+            pp[e >> 1] = pack_bf16(p.x, p.y);
+            pd[e >> 1] = pack_bf16(ds.x, ds.y);
           }
         }
         // P^T and dS^T are free once the previous block's dV, dK products are done
@@ -787,35 +818,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        tmem_st16(tP, pp[0]);
-        tmem_st16(tP + 16, pp[1]);
-        tmem_st16(tDS, pd[0]);
-        tmem_st16(tDS + 16, pd[1]);
+        tmem_st16(tP, pp);
+        tmem_st16(tDS, pd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(ds_full);
       }
       if (!ok) break;
-      // unit end: dV and dK (x 1/8) of this CTA's key rows
+      // unit end: dV and dK (x 1/8) of this CTA's key rows, 16 head columns per warp
       if (!mbar_wait(acc_done, (g - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const size_t row = (size_t)(b * A.S + jb * AB + r) * 3 * d;
-      float v[32];
-      tmem_ld32(tbase + DKV_DV + 32 * half + lane_off, v);
-      store8_bf16_row(A.dqkv + row + 2 * d + h * AD + 32 * half, v, 1.0f);
-      tmem_ld32(tbase + DKV_DK + 32 * half + lane_off, v);
-      store8_bf16_row(A.dqkv + row + d + h * AD + 32 * half, v, 0.125f);
+      float v[16], w[16];
+      tmem_ld16(tbase + DKV_DV + 16 * part + lane_off, v);
+      tmem_ld16(tbase + DKV_DK + 16 * part + lane_off, w);
       tc_fence_before();
       mbar_arrive(o_free);
+      store16_bf16(A.dqkv + row + 2 * d + h * AD + 16 * part, v, 1.0f);
+      store16_bf16(A.dqkv + row + d + h * AD + 16 * part, w, 0.125f);
     }
     if (!ok) fail_wait(A.err, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 16) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, 512);
@@ -827,10 +856,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 //   S = Q K_j^T, dP = dO V_j^T                          TMEM, fp32
 //   dS = 2^(S/8 log2e - LSE log2e) (dP - D)             -> TMEM bf16, two buffers
 //   dQ += dS K_j                                        TMEM, fp32
-// dQ is scaled by 1/8 when it is written out.
-constexpr uint32_t DQ_S = 0, DQ_DP = 128, DQ_DS = 256, DQ_DQ = 384;
+// dQ is scaled by 1/8 when it is written out.  Warps 0-15 elementwise (four
+// per TMEM lane quarter, 32 key columns each, as in the dK/dV kernel), warp 16
+// TMA, warps 17 and 18 MMA issuers.  dQ is accumulated as two halves over the
+// block's keys (keys 0-63 and 64-127, one per issuer, summed when read out):
+// two independent chains of four MMAs instead of one chain of eight.
+constexpr uint32_t DQ_S = 0, DQ_DP = 128, DQ_DS = 256, DQ_DQ = 384, DQ_DQ2 = 448;
+constexpr int DQ_THREADS = 608;
+constexpr int DQ_EW = 512;
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tm_qkv,
                    const __grid_constant__ CUtensorMap tm_do, const AttnArgs A, int nb) {
   extern __shared__ uint8_t smem_raw[];
@@ -857,26 +892,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 2);
-      mbar_init(&ds_full[i], NSWT);
-      mbar_init(&dq_done[i], 1);
+      mbar_init(&ds_full[i], DQ_EW);
+      mbar_init(&dq_done[i], 2);
     }
     for (int i = 0; i < BWD_NST; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 2);
     }
     mbar_init(s_full, 2);
-    mbar_init(s_free, NSWT);
-    mbar_init(o_free, NSWT);
+    mbar_init(s_free, DQ_EW);
+    mbar_init(o_free, DQ_EW);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) tmem_alloc(tmem_slot, 512);
+  if (warp == 16) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 16) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       bool ok = true;
@@ -899,14 +934,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp == 17 || warp == 18) {
     // ---------------- MMA issuers ----------------
-    // Issuer 0 (warp 9): S = Q K_j^T, then dQ += dS K_j; issuer 1 (warp 10):
-    // dP = dO V_j^T.  Issuer 0 issues S of block c + 1 (once the elementwise
-    // warps have read block c's S and dP) before dQ of block c (once they have
-    // written dS of block c).
+    // Issuer 0 (warp 17): S = Q K_j^T, then dQ_lo += dS[:, 0:64] K_j[0:64];
+    // issuer 1 (warp 18): dP = dO V_j^T, then dQ_hi += dS[:, 64:128]
+    // K_j[64:128].  Each issues its S-type product of block c + 1 (once the
+    // elementwise warps have read block c's S and dP) before its dQ half of
+    // block c (once they have written dS of block c).
     if (lane == 0) {
-      const int who = warp - 9;
+      const int who = warp - 17;
       constexpr uint64_t TSTEP = TILE >> 4;
       const uint64_t da0 = who == 0 ? kdesc(sQ, 0) : kdesc(sdO, 0);   // Q or dO
       const uint64_t db0 = who == 0 ? kdesc(sK, 0) : kdesc(sV, 0);    // K_j or V_j
@@ -945,7 +981,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           mma_bf16(t_st, a + kk * 2, bk + kk * 2, IDESC_128x128_KK, kk > 0);
         mma_commit(s_full);
         if (ca.j == ca.ib) mma_commit(&qd_empty[slot]);
-        if (who == 1) mma_commit(&kv_empty[st]);   // V_j is done with once dP is
         advance(ca);
         return true;
       };
@@ -957,38 +992,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tc_fence_after();
         const int st = cb.g % BWD_NST;
         const uint64_t bk = mk0 + (uint64_t)st * TSTEP;
+        const int k0 = 4 * who;                    // this issuer's half of the keys
 #pragma unroll
-        for (int kk = 0; kk < AB / 16; ++kk)
-          mma_bf16_ts(tbase + DQ_DQ, tbase + DQ_DS + 64 * pb + kk * 8, bk + kk * 128,
-                      IDESC_128x64_KMN, kk > 0 || cb.j > 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(tbase + (who == 0 ? DQ_DQ : DQ_DQ2), tbase + DQ_DS + 64 * pb + (k0 + kk) * 8,
+                      bk + (k0 + kk) * 128, IDESC_128x64_KMN, kk > 0 || cb.j > 0);
         mma_commit(&dq_done[pb]);
-        mma_commit(&kv_empty[st]);                 // K_j (S and dQ) is done with
+        mma_commit(&kv_empty[st]);                 // this issuer's use of K_j / V_j is done
         advance(cb);
         return true;
       };
       bool ok = true;
-      if (who == 1) {
-        while (ok && ca.valid) ok = issue_st();
-      } else {
+      if (ca.valid) ok = issue_st();
+      while (ok && cb.valid) {
         if (ca.valid) ok = issue_st();
-        while (ok && cb.valid) {
-          if (ca.valid) ok = issue_st();
-          if (ok) ok = issue_dq();
-        }
+        if (ok) ok = issue_dq();
       }
       if (!ok) fail_wait(A.err, abort_flag);
     }
-  } else if (warp == 11) {
-    // spare warp: each issuing warp keeps an SM sub-partition of its own
-  } else {
-    // ---------------- elementwise: warps 0-7 ----------------
+  } else if (warp < 16) {
+    // ---------------- elementwise: warps 0-15 ----------------
     const int quarter = warp & 3;
-    const int half = warp >> 2;
+    const int part = warp >> 2;                    // key columns 32 part .. +31
     const int r = quarter * 32 + lane;             // query row within the block
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tbase + DQ_S + 64 * half + lane_off;
-    const uint32_t tDP = tbase + DQ_DP + 64 * half + lane_off;
-    const uint32_t tDS = tbase + DQ_DS + 32 * half + lane_off;
+    const uint32_t tS = tbase + DQ_S + 32 * part + lane_off;
+    const uint32_t tDP = tbase + DQ_DP + 32 * part + lane_off;
+    const uint32_t tDS = tbase + DQ_DS + 16 * part + lane_off;
     const float scale2 = LOG2E * 0.125f;
     const float2 sc2 = make_float2(scale2, scale2);
     bool ok = true;
@@ -1004,24 +1034,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        uint32_t sv[2][32], dv[2][32];
-        tmem_ld4x32(tS, tS + 32, tDP, tDP + 32, sv[0], sv[1], dv[0], dv[1]);
+        uint32_t sv[32], dv[32];
+        tmem_ld32_async(tS, sv);
+        tmem_ld32_async(tDP, dv);
+        tmem_wait_regs(sv);
+        reg_fence(dv);
         tc_fence_before();
         mbar_arrive(s_free);                       // S, dP may be overwritten
-        if (j == ib) {
-          mask_diag(sv[0], 64 * half, r);
-          mask_diag(sv[1], 64 * half + 32, r);
-        }
-        uint32_t pd[2][16];
+        if (j == ib) mask_diag(sv, 32 * part, r);
+        uint32_t pd[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 y = __ffma2_rn(u2f2(sv[c][e], sv[c][e + 1]), sc2, nl2);
-            const float2 p = ((e >> 1) & 3) == 3 ? ex2_poly2(y) : make_float2(ex2(y.x), ex2(y.y));
-            const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[c][e], dv[c][e + 1]), nd2));
-            pd[c][e >> 1] = pack_bf16(ds.x, ds.y);
-          }
+        for (int e = 0; e < 32; e += 2) {
+          const float2 y = __ffma2_rn(u2f2(sv[e], sv[e + 1]), sc2, nl2);
+          const float2 p = make_float2(ex2(y.x), ex2(y.y));
+          const float2 ds = __fmul2_rn(p, __fadd2_rn(u2f2(dv[e], dv[e + 1]), nd2));
+          pd[e >> 1] = pack_bf16(ds.x, ds.y);
         }
         // dS[g & 1] was read by the dQ product of block g-2
         const int pb = g & 1;
@@ -1030,32 +1057,34 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        tmem_st16(tDS + 64 * pb, pd[0]);
-        tmem_st16(tDS + 64 * pb + 16, pd[1]);
+        tmem_st16(tDS + 64 * pb, pd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&ds_full[pb]);
       }
       if (!ok) break;
-      // unit end: dQ x 1/8 of this CTA's query rows
+      // unit end: dQ x 1/8 of this CTA's query rows, 16 head columns per warp
       const int gl = g - 1;
       if (!mbar_wait(&dq_done[gl & 1], (gl >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float v[32];
-      tmem_ld32(tbase + DQ_DQ + 32 * half + lane_off, v);
-      store8_bf16_row(A.dqkv + (size_t)(b * A.S + ib * AB + r) * 3 * d + h * AD + 32 * half, v,
-                      0.125f);
+      float v[16], w[16];
+      tmem_ld16(tbase + DQ_DQ + 16 * part + lane_off, v);
+      tmem_ld16(tbase + DQ_DQ2 + 16 * part + lane_off, w);
       tc_fence_before();
       mbar_arrive(o_free);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += w[i];
+      store16_bf16(A.dqkv + (size_t)(b * A.S + ib * AB + r) * 3 * d + h * AD + 16 * part, v,
+                   0.125f);
     }
     if (!ok) fail_wait(A.err, abort_flag);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 16) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, 512);
@@ -1149,8 +1178,8 @@ cudaError_t attn_bwd_tc_launch(const void* qkv, const void* dout, const float* l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int units = (S / AB) * H * nb;
   const int grid = units < sms ? units : sms;
-  attn_bwd_dkdv_tc<<<grid, BWD_THREADS, SMEM_DKDV, s>>>(mq, mo, a, nb);
-  attn_bwd_dq_tc<<<grid, BWD_THREADS, SMEM_DQ, s>>>(mq, mo, a, nb);
+  attn_bwd_dkdv_tc<<<grid, DKV_THREADS, SMEM_DKDV, s>>>(mq, mo, a, nb);
+  attn_bwd_dq_tc<<<grid, DQ_THREADS, SMEM_DQ, s>>>(mq, mo, a, nb);
   return cudaGetLastError();
 }
 
