@@ -105,28 +105,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
   return *reinterpret_cast<uint32_t*>(&hv);
 }
 
-// 2^x for two lanes on the FMA and integer pipes, which the special-function
-// unit's ex2 leaves idle: 2^x = 2^j 2^f with j = round(x) (adding 1.5 * 2^23
-// rounds to an integer and leaves j in the low mantissa bits), f = x - j in
-// [-1/2, 1/2], 2^f from a cubic fitted for least maximum relative error by
-// Lawson's iteratively reweighted least squares (8.4e-5, below bf16 rounding),
-// and j added into the exponent field.  x is clamped below at -125, so keys
-// masked with -inf give ~2^-125 instead of 0: nothing at bf16 resolution.
-__device__ __forceinline__ float2 ex2_poly2(float2 x) {
-  constexpr float RND = 12582912.0f;
-  constexpr float C0 = 0.999919593334198f, C1 = 0.6932621598243713f,
-                  C2 = 0.24271413683891296f, C3 = 0.055212993174791336f;
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 t = __fadd2_rn(x, make_float2(RND, RND));
-  const float2 j = __fadd2_rn(t, make_float2(-RND, -RND));
-  const float2 f = __ffma2_rn(j, make_float2(-1.0f, -1.0f), x);
-  float2 p = __ffma2_rn(make_float2(C3, C3), f, make_float2(C2, C2));
-  p = __ffma2_rn(p, f, make_float2(C1, C1));
-  p = __ffma2_rn(p, f, make_float2(C0, C0));
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
 
 // 32 fp32 S values (raw bits) of row r at columns col0.. : keys after the
 // query get -inf when the block is the diagonal one.
@@ -533,7 +511,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // elementwise work (warp w: TMEM lane quarter w & 3, columns 64 (w >> 2) ..
 // +63), S and dP read from TMEM once and released, and the bf16 products P /
 // dS written back into TMEM as the A operand of the accumulating MMAs.
-constexpr int BWD_THREADS = 384;   // warps 0-7 elementwise, 8 TMA, 9-10 MMA, 11 spare
 constexpr int BWD_NST = 3;   // ring stages of the streamed operand pair
 
 __device__ __forceinline__ bool bwd_unit(int k, int n_units, int hb, int H, int& major, int& h,
@@ -555,19 +532,6 @@ __device__ __forceinline__ void mask_diag_t(uint32_t (&v)[32], int col0, int r) 
     if (col0 + e < r) v[e] = 0xff800000u;
 }
 
-// Four 32-column TMEM loads of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld4x32(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3,
-                                            uint32_t (&a)[32], uint32_t (&b)[32],
-                                            uint32_t (&c)[32], uint32_t (&e)[32]) {
-  tmem_ld32_async(t0, a);
-  tmem_ld32_async(t1, b);
-  tmem_ld32_async(t2, c);
-  tmem_ld32_async(t3, e);
-  tmem_wait_regs(a);
-  reg_fence(b);
-  reg_fence(c);
-  reg_fence(e);
-}
 
 
 // ------------------------------------------------------------ dK / dV
