@@ -32,14 +32,27 @@ __device__ __forceinline__ float ldg_or0(const T* p, long long i, bool ok) {
   return ok ? ld_elem(p, (size_t)i) : 0.0f;
 }
 
-template <typename T, bool A_MN, bool B_K>
-__device__ __forceinline__ void load_tiles(const GemmArgs& g, int m0, int n0, int k0, int tid,
-                                           float ra[8], float rb[8]) {
+// Eight consecutive fp32 elements as two 16-byte loads when they are in
+// bounds and 16-byte aligned (false: load them element by element).
+__device__ __forceinline__ bool load8_vec(const float* p, long long i, bool all_in, float r[8]) {
+  const float* q = p + i;
+  if (!all_in || (reinterpret_cast<uintptr_t>(q) & 15) != 0) return false;
+  const float4 u = reinterpret_cast<const float4*>(q)[0];
+  const float4 v = reinterpret_cast<const float4*>(q)[1];
+  r[0] = u.x; r[1] = u.y; r[2] = u.z; r[3] = u.w;
+  r[4] = v.x; r[5] = v.y; r[6] = v.z; r[7] = v.w;
+  return true;
+}
+__device__ __forceinline__ bool load8_vec(const bf16*, long long, bool, float*) { return false; }
+
+// The eight consecutive elements of A (or B) a thread stages per K tile.
+template <typename T, bool A_MN>
+__device__ __forceinline__ void load_a(const GemmArgs& g, int m0, int k0, int tid, float ra[8]) {
   const T* A = static_cast<const T*>(g.A);
-  const T* B = static_cast<const T*>(g.B);
   if (A_MN) {  // A[k*lda + m]: 16 k-rows x 128 m, 8 consecutive m per thread
     int k = tid >> 4, mm = (tid & 15) * 8;
     int gk = k0 + k;
+    if (load8_vec(A, (long long)gk * g.lda + m0 + mm, gk < g.K && m0 + mm + 8 <= g.M, ra)) return;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       int gm = m0 + mm + i;
@@ -48,15 +61,22 @@ __device__ __forceinline__ void load_tiles(const GemmArgs& g, int m0, int n0, in
   } else {  // A[m*lda + k]: 128 m-rows x 16 k, 8 consecutive k per thread
     int m = tid >> 1, kk = (tid & 1) * 8;
     int gm = m0 + m;
+    if (load8_vec(A, (long long)gm * g.lda + k0 + kk, gm < g.M && k0 + kk + 8 <= g.K, ra)) return;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       int gk = k0 + kk + i;
       ra[i] = ldg_or0(A, (long long)gm * g.lda + gk, gk < g.K && gm < g.M);
     }
   }
+}
+
+template <typename T, bool B_K>
+__device__ __forceinline__ void load_b(const GemmArgs& g, int n0, int k0, int tid, float rb[8]) {
+  const T* B = static_cast<const T*>(g.B);
   if (!B_K) {  // B[k*ldb + n]
     int k = tid >> 4, nn = (tid & 15) * 8;
     int gk = k0 + k;
+    if (load8_vec(B, (long long)gk * g.ldb + n0 + nn, gk < g.K && n0 + nn + 8 <= g.N, rb)) return;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       int gn = n0 + nn + i;
@@ -65,12 +85,20 @@ __device__ __forceinline__ void load_tiles(const GemmArgs& g, int m0, int n0, in
   } else {  // B[n*ldb + k]
     int n = tid >> 1, kk = (tid & 1) * 8;
     int gn = n0 + n;
+    if (load8_vec(B, (long long)gn * g.ldb + k0 + kk, gn < g.N && k0 + kk + 8 <= g.K, rb)) return;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       int gk = k0 + kk + i;
       rb[i] = ldg_or0(B, (long long)gn * g.ldb + gk, gk < g.K && gn < g.N);
     }
   }
+}
+
+template <typename T, bool A_MN, bool B_K>
+__device__ __forceinline__ void load_tiles(const GemmArgs& g, int m0, int n0, int k0, int tid,
+                                           float ra[8], float rb[8]) {
+  load_a<T, A_MN>(g, m0, k0, tid, ra);
+  load_b<T, B_K>(g, n0, k0, tid, rb);
 }
 
 template <bool A_MN, bool B_K>
@@ -131,8 +159,21 @@ __device__ __forceinline__ void dot2_step(float a, float b, float& s, float& c) 
   c = __fadd_rn(c, __fadd_rn(pe, se));
 }
 
+// Two CTAs per SM for the plain kernel (128 registers, four warps per SM
+// sub-partition to hide the FFMA latency chains); the compensated kernel
+// keeps its 128 accumulators and their error terms in registers at one CTA.
+// A strict weight gradient split over K (blockIdx.z = split, k_per > 0)
+// writes its partial tile to its slice of split_ws.
 template <typename T, typename TO, typename TX, bool A_MN, bool B_K, bool COMP>
-__global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(NT, COMP ? 1 : 2) gemm_simt_kernel(const GemmArgs gin, int k_per) {
+  GemmArgs g = gin;
+  int k_lo = 0;
+  if (k_per > 0) {
+    k_lo = blockIdx.z * k_per;
+    g.K = min(gin.K, k_lo + k_per);
+    g.out = gin.split_ws + (size_t)blockIdx.z * gin.M * gin.N;
+    g.ldo = gin.N;
+  }
   __shared__ __align__(16) float As[2][BK][BM + PAD];
   __shared__ __align__(16) float Bs[2][BK][BN + PAD];
   const int tid = threadIdx.x;
@@ -164,15 +205,15 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
   const float* epi_bias = COMP ? nullptr : g.bias;
 
   float ra[8], rb[8];
-  load_tiles<T, A_MN, B_K>(g, m0, n0, 0, tid, ra, rb);
+  load_tiles<T, A_MN, B_K>(g, m0, n0, k_lo, tid, ra, rb);
   store_tiles<A_MN, B_K>(As[0], Bs[0], tid, ra, rb);
   __syncthreads();
 
-  const int nk = (g.K + BK - 1) / BK;
+  const int nk = (g.K - k_lo + BK - 1) / BK;
   for (int kt = 0; kt < nk; ++kt) {
     const int cur = kt & 1;
     const bool more = kt + 1 < nk;
-    if (more) load_tiles<T, A_MN, B_K>(g, m0, n0, (kt + 1) * BK, tid, ra, rb);
+    if (more) load_tiles<T, A_MN, B_K>(g, m0, n0, k_lo + (kt + 1) * BK, tid, ra, rb);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[8], b[8];
@@ -716,11 +757,68 @@ cudaError_t gemm_skinny(const GemmArgs& g, int kind, cudaStream_t s) {
 template <typename T, typename TO, typename TX, bool A_MN, bool B_K, bool COMP = false>
 cudaError_t launch1(const GemmArgs& g, cudaStream_t s) {
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
-  gemm_simt_kernel<T, TO, TX, A_MN, B_K, COMP><<<grid, NT, 0, s>>>(g);
+  gemm_simt_kernel<T, TO, TX, A_MN, B_K, COMP><<<grid, NT, 0, s>>>(g, 0);
+  return cudaGetLastError();
+}
+
+// Splits of a strict weight gradient (fp32 operands and output, no epilogue)
+// whose 128x128 tiles leave SMs idle: enough splits to give about two CTAs
+// per SM, at most 8, each at least 256 deep in K.
+int strict_dw_splits(const GemmArgs& g) {
+  if (!(g.in_type == DT_F32 && g.a_mn && !g.b_k && g.out_type == DT_F32 && !g.bias && !g.act &&
+        !g.out_z && !g.dact && !g.resid))
+    return 1;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  int sp = (2 * sms + tiles - 1) / tiles;
+  if (sp > 8) sp = 8;
+  while (sp > 1 && g.K / sp < 256) --sp;
+  return sp;
+}
+
+// out = sum over splits of the partial tiles, in split order.
+__global__ void __launch_bounds__(256) split_sum_kernel(const float* ws, int splits, int M, int N,
+                                                       float* out, long long ldo) {
+  const size_t mn = (size_t)M * N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < mn;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float v = ws[i];
+    for (int s = 1; s < splits; ++s) v += ws[(size_t)s * mn + i];
+    out[(i / N) * ldo + (i % N)] = v;
+  }
+}
+
+cudaError_t launch_strict_dw_split(const GemmArgs& g, int splits, cudaStream_t s) {
+  const int k_per = ((g.K + splits - 1) / splits + BK - 1) / BK * BK;
+  const int used = (g.K + k_per - 1) / k_per;
+  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, used);
+  gemm_simt_kernel<float, float, float, true, false, false><<<grid, NT, 0, s>>>(g, k_per);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t mn = (size_t)g.M * g.N;
+  int blocks = (int)((mn + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  split_sum_kernel<<<blocks, 256, 0, s>>>(g.split_ws, used, g.M, g.N, static_cast<float*>(g.out),
+                                          g.ldo);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t gemm_simt_split_floats(const GemmArgs& g) {
+  int kind = 0;
+  if (g.M <= 0 || g.N <= 0 || skinny_kind(g, &kind)) return 0;
+  if (g.a_mn && !g.b_k && g.N <= 32) return 0;                 // narrow weight gradient
+  if ((long long)g.M * g.N <= 65536 && g.K >= 64) return 0;    // warp per output
+  const int sp = strict_dw_splits(g);
+  return sp > 1 ? (size_t)sp * g.M * g.N : 0;
+}
 
 bool gemm_simt_skinny(const GemmArgs& g) {
   int kind = 0;
@@ -749,7 +847,12 @@ cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.in_type == DT_F32) {   // strict path: everything fp32
     if (!g.a_mn && !g.b_k) return launch1<float, float, float, false, false, true>(g, s);
     if (!g.a_mn && g.b_k) return launch1<float, float, float, false, true>(g, s);
-    if (g.a_mn && !g.b_k) return launch1<float, float, float, true, false>(g, s);
+    if (g.a_mn && !g.b_k) {
+      const int sp = strict_dw_splits(g);
+      if (sp > 1 && g.split_ws && (size_t)sp * g.M * g.N <= g.split_ws_floats)
+        return launch_strict_dw_split(g, sp, s);
+      return launch1<float, float, float, true, false>(g, s);
+    }
     return cudaErrorNotSupported;
   }
   if (g.out_type == DT_F32) {

@@ -35,9 +35,15 @@ struct GemmArgs {
   // columns below N, y = x log2(e), x the value as stored (bias added, rounded
   // to out_type).
   float2* lse_part = nullptr; int lse_ld = 0;
+  // Scratch for the strict weight-gradient GEMM's split over K (floats), or
+  // null: each split writes its partial tile there and one pass adds the
+  // splits in order (deterministic, unlike atomics).
+  float* split_ws = nullptr; size_t split_ws_floats = 0;
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
+// Floats of split_ws gemm_simt uses for g (0: g is not split).
+size_t gemm_simt_split_floats(const GemmArgs& g);
 // Whether gemm_simt runs g on its narrow-side bf16 kernels (N <= 32 forward
 // or weight gradient, K <= 32 input gradient).
 bool gemm_simt_skinny(const GemmArgs& g);

@@ -103,6 +103,7 @@ struct mg_plan {
   char* ws = nullptr;
   size_t shadow_off = 0, chunks_off = 0, loss_off = 0, rowloss_off = 0, partial_off = 0,
          colsum_off = 0, flag_off = 0, lse_part_off = 0;
+  size_t split_off = 0, split_floats = 0;   // strict weight gradients split over K
   int lse_parts = 0;         // 128-column softmax partials per logits row (0: not planned)
   int n_chunks = 0;
   const float* last_params = nullptr;
@@ -433,6 +434,10 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
       g.B = gy; g.ldb = n.d_out; g.b_k = 0;
       g.in_type = dt; g.aux_type = dt;
       g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
+      if (p->split_floats) {
+        g.split_ws = wsp<float>(p, p->split_off);
+        g.split_ws_floats = p->split_floats;
+      }
       if (n.has_bias) {
         // db = column sums of dZ, on the auxiliary stream (only the optimizer
         // reads it), overlapping this node's dW and dX products
@@ -827,6 +832,19 @@ void layout_workspace(mg_plan* p) {
   if (part < (size_t)kMsePartials * 4) part = (size_t)kMsePartials * 4;
   p->partial_off = b.take(part);
   p->colsum_off = b.take(kColsumFloats * 4);   // the bias-gradient sums' own partials (aux stream)
+  // partial tiles of strict weight gradients split over K (main stream only,
+  // one at a time): the largest any linear node needs
+  p->split_floats = 0;
+  if (p->dt == DT_F32) {
+    for (const Node& n : p->nodes) {
+      if (n.kind != NK_LINEAR) continue;
+      GemmArgs g;
+      g.M = n.d_in; g.N = n.d_out; g.K = p->batch;
+      g.a_mn = 1; g.b_k = 0; g.in_type = DT_F32; g.out_type = DT_F32;
+      p->split_floats = std::max(p->split_floats, gemm_simt_split_floats(g));
+    }
+  }
+  p->split_off = b.take(p->split_floats * 4);
   // softmax partials of a cross-entropy head computed by a tensor-core GEMM
   const Value& fv = p->values[p->final_value];
   if (p->dt == DT_BF16 && p->loss != MG_LOSS_MSE && fv.width % 8 == 0 && fv.producer >= 0 &&
