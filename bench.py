@@ -30,11 +30,12 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
 # kernel family, averaged over the launches of one training step, from one ncu
 # capture of the current code (summary and command under profiles/); keyed by
-# (workload, family); None when not captured for that pair, or when the
-# kernel has changed since its capture.  The C3 SM-pair figure under profiles/
-# (249.5 MB per launch over ten launches) predates the pair kernel's split-K
-# and the head weight gradient joining the family, so it is not reported.
-TRAFFIC = {}
+# (workload, family); absent when not captured for that pair, or when the
+# kernel has changed since its capture.
+TRAFFIC = {
+    # profiles/gemm_pair_c3_step_dram_traffic.md: eleven launches of one step
+    ("c3_mlp4096_gelu", "gemm_pair_kernel (tcgen05 cta_group::2)"): 234.6e6,
+}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
