@@ -125,7 +125,10 @@ mg_status mg_param_info(const mg_plan* plan, int i, size_t* offset, int* rows, i
  * lifetime sharing of gradient buffers (abstract of "Meganeura: Portable GPU
  * Training and Inference through Vulkan and Metal": memory planner; README,
  * Environment variables section: buffer lifetime aliasing, off with
- * MG_NO_ALIAS=1 here). */
+ * MG_NO_ALIAS=1 here).  With MG_RECOMPUTE_GELU=1 at plan creation the GELU
+ * pre-activations are not kept: the backward recomputes each one (the
+ * forward's GEMM again, same inputs and weights, same result) into a single
+ * shared buffer just before the input-gradient GEMM that needs it. */
 size_t mg_workspace_bytes(const mg_plan* plan);
 
 /* Forward pass only: the inference side of the train-to-deploy stack (README,

@@ -110,6 +110,11 @@ struct mg_plan {
   bool use_tc = true;        // tcgen05 GEMMs in bf16 mode (MG_GEMM=simt turns them off)
   bool use_pair = true;      // SM-pair GEMMs for large shapes (MG_GEMM=tc1 turns them off)
   bool alias = true;         // gradient buffers share storage by lifetime (MG_NO_ALIAS=1: not)
+  // GELU pre-activations recomputed in the backward instead of saved
+  // (MG_RECOMPUTE_GELU=1): the forward does not store Z; one Z-sized buffer,
+  // shared by every GELU layer, receives Z = X W + b again just before the
+  // input-gradient GEMM that needs GELU'(Z)
+  bool recompute_gelu = false;
   // CUDA-graph replay of the training step (MG_GRAPH=0: every kernel launched
   // directly): a step is captured on the second call with the same buffers
   // and relaunched with the optimizer nodes' step scalars updated; graphs for
@@ -297,7 +302,7 @@ void forward_pass(Exec& e, const float* params, const void* x) {
       g.in_type = dt;
       g.bias = n.has_bias ? params + n.b_off : nullptr;
       g.act = n.act;
-      if (n.z >= 0) { g.out_z = p->ws + p->values[n.z].off; g.ldz = n.d_out; }
+      if (n.z >= 0 && !p->recompute_gelu) { g.out_z = p->ws + p->values[n.z].off; g.ldz = n.d_out; }
       if (n.skip >= 0) { g.resid = val_ptr(p, n.skip, x); g.ldr = n.d_out; }
       g.aux_type = dt;
       g.out = p->ws + p->values[n.out].off; g.ldo = n.d_out; g.out_type = dt;
@@ -468,6 +473,22 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
           int sv = vin.producer_act == ACT_GELU ? vin.z_value : n.in;
           h.saved = p->ws + p->values[sv].off;
           h.lds = n.d_in;
+          if (vin.producer_act == ACT_GELU && p->recompute_gelu) {
+            // Z of the producing Linear again, exactly as its forward GEMM
+            // formed it (same kernel, inputs and weights: the optimizer has
+            // not yet updated that node), into the shared Z buffer
+            const Node& pn = p->nodes[vin.producer];
+            GemmArgs r;
+            r.M = p->batch; r.N = pn.d_out; r.K = pn.d_in;
+            r.A = val_ptr(p, pn.in, x); r.lda = pn.d_in; r.a_mn = 0;
+            r.B = (const char*)wbase + pn.w_off * dtype_size(dt); r.ldb = pn.d_out; r.b_k = 0;
+            r.in_type = dt;
+            r.bias = pn.has_bias ? params + pn.b_off : nullptr;
+            r.aux_type = dt;
+            r.out = p->ws + p->values[pn.z].off; r.ldo = pn.d_out; r.out_type = dt;
+            site(e, gemm_name(p, "recompute_z", pn.layer, r), 2.0 * r.M * r.N * r.K, gemm_bytes(r),
+                 1, [&] { return run_gemm(p, r, e.s); });
+          }
         }
         if (dadd) { h.resid = dadd; h.ldr = n.d_in; }
         h.out = grad_ptr(p, n.in); h.ldo = n.d_in; h.out_type = dt;
@@ -802,9 +823,20 @@ void layout_workspace(mg_plan* p) {
   Bump b;
   const size_t es = dtype_size(p->dt);
   const size_t B = (size_t)p->batch;
+  // saved GELU pre-activations: their own buffers, or one shared buffer that
+  // the backward refills (MG_RECOMPUTE_GELU=1)
+  std::vector<char> is_z(p->values.size(), 0);
+  size_t zmax = 0;
+  for (const Node& n : p->nodes)
+    if (n.z >= 0) {
+      is_z[n.z] = 1;
+      zmax = std::max(zmax, (size_t)p->values[n.z].width);
+    }
+  size_t zshared = 0;
+  if (p->recompute_gelu && zmax) zshared = b.take(B * zmax * es);
   for (size_t i = 1; i < p->values.size(); ++i) {
     Value& v = p->values[i];
-    v.off = b.take(B * v.width * es);
+    v.off = (p->recompute_gelu && is_z[i]) ? zshared : b.take(B * v.width * es);
   }
   plan_gradients(p, b);
   // x's gradient is never formed; a value's need_grad is false for x
@@ -887,6 +919,7 @@ void build_dump(mg_plan* p) {
   snprintf(b, sizeof b, "  gradient storage: %zu bytes (%zu without lifetime sharing%s)\n",
            p->grad_bytes, p->grad_bytes_unaliased, p->alias ? "" : "; MG_NO_ALIAS set");
   s += b;
+  if (p->recompute_gelu) s += "  GELU pre-activations: recomputed in the backward (MG_RECOMPUTE_GELU set)\n";
   for (size_t i = 0; i < p->p_off.size(); ++i) {
     snprintf(b, sizeof b, "  param %zu: offset %zu [%d x %d]\n", i, p->p_off[i], p->p_rows[i],
              p->p_cols[i]);
@@ -1068,6 +1101,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     p->use_pair = p->use_tc && strcmp(ev, "tc1") != 0;
   }
   if (const char* ev = getenv("MG_NO_ALIAS")) p->alias = !(ev[0] == '1' && ev[1] == 0);
+  if (const char* ev = getenv("MG_RECOMPUTE_GELU")) p->recompute_gelu = ev[0] == '1' && ev[1] == 0;
   if (const char* ev = getenv("MG_GRAPH")) p->use_graph = !(ev[0] == '0' && ev[1] == 0);
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
