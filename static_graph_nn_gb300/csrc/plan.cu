@@ -115,6 +115,11 @@ struct mg_plan {
   // shared by every GELU layer, receives Z = X W + b again just before the
   // input-gradient GEMM that needs GELU'(Z)
   bool recompute_gelu = false;
+  // A linear node whose weight gradient (and update) is moved to the end of
+  // the backward: the smallest one, when it is smaller than the node the
+  // backward ends with.  The last node's update has nothing left to overlap,
+  // so the step ends with the smallest update instead of the last layer's.
+  int defer_dw = -1;
   // CUDA-graph replay of the training step (MG_GRAPH=0: every kernel launched
   // directly): a step is captured on the second call with the same buffers
   // and relaunched with the optimizer nodes' step scalars updated; graphs for
@@ -425,6 +430,7 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
   mg_plan* p = e.p;
   const DType dt = p->dt;
   const void* wbase = dt == DT_BF16 ? (const void*)(p->ws + p->shadow_off) : (const void*)params;
+  GemmArgs deferred;   // the deferred node's weight gradient
   for (int ni = (int)p->nodes.size() - 1; ni >= 0; --ni) {
     const Node& n = p->nodes[ni];
     if (!p->values[n.out].need_grad) continue;
@@ -459,8 +465,12 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
                                 kColsumFloats, grads + n.b_off, p->aux);
                 });
       }
-      site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
-           [&] { return run_gemm(p, g, e.s); });
+      if (ni == p->defer_dw) {
+        deferred = g;
+      } else {
+        site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
+             [&] { return run_gemm(p, g, e.s); });
+      }
       if (vin.need_grad) {
         // dX = dZ W^T, times act'(saved) of the producer of X, plus the skip gradient
         GemmArgs h;
@@ -495,7 +505,7 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
         site(e, gemm_name(p, "dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
              [&] { return run_gemm(p, h, e.s); });
       }
-      node_update(e, ni);
+      if (ni != p->defer_dw) node_update(e, ni);
     } else if (n.kind == NK_RMSNORM) {
       void* dx = vin.need_grad ? grad_ptr(p, n.in) : nullptr;
       double bytes = (double)dtype_size(dt) * p->batch * n.d * (dx ? (dadd ? 4 : 3) : 2);
@@ -531,6 +541,12 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
                         wsp<float>(p, n.dsum_off), grad_ptr(p, n.in), nb, n.S, n.nh, n.dh, e.s);
       });
     }
+  }
+  if (p->defer_dw >= 0) {
+    const Node& n = p->nodes[p->defer_dw];
+    site(e, gemm_name(p, "dW", n.layer, deferred), 2.0 * deferred.M * deferred.N * deferred.K,
+         gemm_bytes(deferred), 1, [&] { return run_gemm(p, deferred, e.s); });
+    node_update(e, p->defer_dw);
   }
 }
 
@@ -778,6 +794,7 @@ void plan_gradients(mg_plan* p, Bump& b) {
       const Node& pr = p->nodes[v.producer];
       f.end = std::max(f.end, pos(v.producer));
       if (pr.kind == NK_LINEAR && pr.has_bias) f.end = kForever;
+      if (v.producer == p->defer_dw) f.end = kForever;   // read by the deferred weight gradient
     }
     for (int ni = 0; ni < N; ++ni)
       if (p->values[p->nodes[ni].in].pending_add == (int)vi) f.end = std::max(f.end, pos(ni));
@@ -819,7 +836,22 @@ void plan_gradients(mg_plan* p, Bump& b) {
   }
 }
 
+// The weight gradient moved to the end of the backward (see mg_plan::defer_dw).
+int choose_deferred_dw(const mg_plan* p) {
+  int last = -1, smallest = -1;
+  auto wcount = [&](int ni) { return (double)p->nodes[ni].d_in * p->nodes[ni].d_out; };
+  for (int ni = 0; ni < (int)p->nodes.size(); ++ni) {
+    const Node& n = p->nodes[ni];
+    if (n.kind != NK_LINEAR || !p->values[n.out].need_grad) continue;
+    if (last < 0) last = ni;                    // the backward processes it last
+    if (smallest < 0 || wcount(ni) < wcount(smallest)) smallest = ni;
+  }
+  if (smallest < 0 || smallest == last || wcount(smallest) >= wcount(last)) return -1;
+  return smallest;
+}
+
 void layout_workspace(mg_plan* p) {
+  p->defer_dw = choose_deferred_dw(p);
   Bump b;
   const size_t es = dtype_size(p->dt);
   const size_t B = (size_t)p->batch;
