@@ -165,7 +165,11 @@ mg_status mg_forward(mg_plan* plan, const float* params, const void* x, float* o
  * inputs).  Results are the same as launching each kernel.  Not used while
  * profiling or when `stream` is itself being captured; the environment
  * variable MG_GRAPH=0, read at plan creation, turns it off.  If a capture
- * fails the plan launches directly from then on. */
+ * fails the plan launches directly from then on.
+ * With MG_FUSED_UPDATE=1 at plan creation (Adam, bf16) a weight whose
+ * gradient GEMM runs on the tensor cores without a split over K is updated in
+ * that GEMM's epilogue instead of the optimizer kernel: same results, one
+ * launch fewer per such layer. */
 mg_status mg_train_step(mg_plan* plan, float* params, float* grads, float* adam_m,
                         float* adam_v, const void* x, const void* labels, float lr, int step,
                         mg_stream_t stream);

@@ -112,4 +112,107 @@ __device__ __forceinline__ void softmax_partial32(const GemmArgs& g, int n0, con
   ps += acc;
 }
 
+// Column sums over a warp's 32 rows: lane l holds row l's 32 consecutive
+// columns in x; returns the sum of column l over the 32 lanes.  A butterfly
+// reduce-scatter: at each of five steps every lane keeps one half of its
+// remaining columns (the upper half if its lane bit is set), sends the other
+// half to the partner lane and adds what it receives, so the additions run
+// in a fixed order (deterministic).  x is clobbered.
+__device__ __forceinline__ float warp_colsum32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = up ? x[j] : x[j + w];
+      const float keep = up ? x[j + w] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return x[0];
+}
+
+// Bias-gradient partials of one epilogue chunk (GemmArgs::col_part): v holds
+// this lane's row (row m of a 32-row group starting at a multiple of 32) at
+// columns n0 .. n0+31 as computed before the final rounding; rows at or
+// beyond M and columns at or beyond N count as zero.  All 32 lanes call it.
+template <typename TO>
+__device__ __forceinline__ void col_partial32(const GemmArgs& g, int m, int n0, int lane,
+                                              float (&v)[32]) {
+  const bool row_ok = m < g.M;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float r = sizeof(TO) == 2 ? __bfloat162float(__float2bfloat16_rn(v[j])) : v[j];
+    v[j] = row_ok && n0 + j < g.N ? r : 0.0f;
+  }
+  const float t = warp_colsum32(v, lane);
+  if (n0 + lane < g.N) g.col_part[(size_t)(m >> 5) * g.N + n0 + lane] = t;
+}
+
+// One Adam step of one parameter (t = step, 1-based; lr_bc1 = lr / (1 - b1^t),
+// inv_sqrt_bc2 = 1 / sqrt(1 - b2^t)): m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2,
+// p -= lr_bc1 m / (sqrt(v) inv_sqrt_bc2 + eps).  Shared by the optimizer
+// kernel and the weight-gradient epilogue, so both give the same bits.
+__device__ __forceinline__ void adam_one(float& p, float g, float& m, float& v, float lr_bc1,
+                                         float inv_sqrt_bc2, float b1, float b2, float eps) {
+  m = b1 * m + (1.0f - b1) * g;
+  v = b2 * v + (1.0f - b2) * g * g;
+  p -= lr_bc1 * m / (sqrtf(v) * inv_sqrt_bc2 + eps);
+}
+
+// Adam update fused into a weight-gradient epilogue (GemmArgs::upd_p set):
+// gr holds the fp32 gradients of row m, columns n0 .. n0+31 (as stored in
+// out); the parameters, moments and bf16 copy share out's layout.
+__device__ __forceinline__ void adam_update32(const GemmArgs& g, bool vec, int m, int n0,
+                                              const float (&gr)[32]) {
+  const float lr_bc1 = g.upd_scal[0], inv = g.upd_scal[1];
+  const float b1 = g.upd_b1, b2 = g.upd_b2, eps = g.upd_eps;
+  const size_t base = (size_t)m * g.ldo + n0;
+  if (vec && n0 + 32 <= g.N) {
+    float4* p4 = reinterpret_cast<float4*>(g.upd_p + base);
+    float4* m4 = reinterpret_cast<float4*>(g.upd_m + base);
+    float4* v4 = reinterpret_cast<float4*>(g.upd_v + base);
+    uint2* s4 = reinterpret_cast<uint2*>(static_cast<bf16*>(g.upd_shadow) + base);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {   // 16 columns at a time: their 12 loads in flight together
+      float4 pp[4], mm[4], vv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        pp[q] = p4[4 * h + q];
+        mm[q] = m4[4 * h + q];
+        vv[q] = v4[4 * h + q];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float* gq = gr + 16 * h + 4 * q;
+        adam_one(pp[q].x, gq[0], mm[q].x, vv[q].x, lr_bc1, inv, b1, b2, eps);
+        adam_one(pp[q].y, gq[1], mm[q].y, vv[q].y, lr_bc1, inv, b1, b2, eps);
+        adam_one(pp[q].z, gq[2], mm[q].z, vv[q].z, lr_bc1, inv, b1, b2, eps);
+        adam_one(pp[q].w, gq[3], mm[q].w, vv[q].w, lr_bc1, inv, b1, b2, eps);
+        p4[4 * h + q] = pp[q];
+        m4[4 * h + q] = mm[q];
+        v4[4 * h + q] = vv[q];
+        __nv_bfloat162 lo = __floats2bfloat162_rn(pp[q].x, pp[q].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(pp[q].z, pp[q].w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        s4[4 * h + q] = u;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (n0 + j >= g.N) continue;
+    const size_t k = base + j;
+    float pp = g.upd_p[k], mm = g.upd_m[k], vv = g.upd_v[k];
+    adam_one(pp, gr[j], mm, vv, lr_bc1, inv, b1, b2, eps);
+    g.upd_p[k] = pp;
+    g.upd_m[k] = mm;
+    g.upd_v[k] = vv;
+    static_cast<bf16*>(g.upd_shadow)[k] = __float2bfloat16_rn(pp);
+  }
+}
+
 }  // namespace mg

@@ -71,6 +71,8 @@ __device__ __forceinline__ void store8_bf16(bf16* p, const float* f) {
 
 // Epilogue of 32 consecutive columns of one row (same rounding points as the
 // CUDA-core GEMM's epilogue).  Full, aligned chunks move in 16-byte vectors.
+// On return v holds the values stored (before their rounding to TO) at the
+// columns below N.
 template <typename TO>
 __device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int m, int n0,
                                                float (&v)[32]) {
@@ -147,6 +149,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int 
     }
     if (g.resid) x += __bfloat162float(static_cast<const bf16*>(g.resid)[rr + n]);
     st_elem(static_cast<TO*>(g.out), (size_t)m * g.ldo + n, x);
+    v[j] = x;
   }
 }
 
@@ -311,8 +314,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           } else {
             if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
             epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+            if (sizeof(TO) == 4 && P.g.upd_p) adam_update32(P.g, P.vec != 0, m, n0 + c * 32, v);
           }
         }
+        // warp-uniform: the warp's 32-row group starts below M, the chunk below N
+        if (P.g.col_part && (m & ~31) < P.g.M && n0 + c * 32 < P.g.N)
+          col_partial32<TO>(P.g, m, n0 + c * 32, lane, v);
       }
       if (P.g.lse_part && m < P.g.M && n0 + half * (BN / 2) < P.g.N)
         P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (BN / 2)) / 128] = make_float2(pm, ps);
@@ -399,7 +406,7 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
     auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
     P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) &&
-            (lds & 7) == 0;
+            al(g.upd_p) && al(g.upd_m) && al(g.upd_v) && al(g.upd_shadow) && (lds & 7) == 0;
   }
   const size_t smem = 1024 + (size_t)STAGES * (TC_BM + BN) * TC_BK * 2 + (2 * STAGES + 4) * 8 + 16;
   auto kern = gemm_tc_kernel<BN, STAGES, TO, A_MN, B_MN>;
@@ -452,7 +459,8 @@ int gemm_tc_splits(const GemmArgs& g, double* steps) {
   const int sms = num_sms();
   const int tiles = ((g.M + TC_BM - 1) / TC_BM) * ((g.N + 255) / 256);
   const int kb = (g.K + TC_BK - 1) / TC_BK;
-  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid &&
+                     !g.col_part && !g.upd_p;
   int splits = 1;
   double best = (double)((tiles + sms - 1) / sms);
   if (plain && tiles < sms) {

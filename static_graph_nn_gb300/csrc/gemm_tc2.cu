@@ -145,7 +145,9 @@ __device__ __forceinline__ void split_add32(const GemmArgs& g, bool vec, int m, 
     if (n0 + j < g.N) atomicAdd(out + j, v[j]);
 }
 
-// Epilogue of 32 columns of one row; identical arithmetic to gemm_tc.cu.
+// Epilogue of 32 columns of one row; identical arithmetic to gemm_tc.cu.  On
+// return v holds the values stored (before their rounding to TO) at the
+// columns below N.
 template <typename TO>
 __device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, int m, int n0, float (&v)[32]) {
   if (vec && n0 + 32 <= g.N) {
@@ -217,6 +219,7 @@ __device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, int m, int n0
     }
     if (g.resid) x += __bfloat162float(static_cast<const bf16*>(g.resid)[rr + n]);
     st_elem(static_cast<TO*>(g.out), (size_t)m * g.ldo + n, x);
+    v[j] = x;
   }
 }
 
@@ -365,8 +368,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           } else {
             if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
             epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+            if (sizeof(TO) == 4 && P.g.upd_p) adam_update32(P.g, P.vec != 0, m, n0 + c * 32, v);
           }
         }
+        // warp-uniform: the warp's 32-row group starts below M, the chunk below N
+        if (P.g.col_part && (m & ~31) < P.g.M && n0 + c * 32 < P.g.N)
+          col_partial32<TO>(P.g, m, n0 + c * 32, lane, v);
       }
       if (P.g.lse_part && m < P.g.M && n0 + half * (P_BN / 2) < P.g.N)
         P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (P_BN / 2)) / 128] = make_float2(pm, ps);
@@ -469,7 +476,8 @@ int pair_splits(const GemmArgs& g, double* steps) {
   const int slots = pair_slots();
   const int tiles = ((g.M + 2 * P_BM - 1) / (2 * P_BM)) * ((g.N + P_BN - 1) / P_BN);
   const int kb = (g.K + P_BK - 1) / P_BK;
-  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid;
+  const bool plain = g.out_type == DT_F32 && !g.bias && !g.act && !g.out_z && !g.dact && !g.resid &&
+                     !g.col_part && !g.upd_p;
   int splits = 1;
   double best = (double)((tiles + slots - 1) / slots);
   if (plain && tiles < slots) {
@@ -509,7 +517,8 @@ cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
   {
     auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
-    P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) && (lds & 7) == 0;
+    P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) && al(g.upd_p) &&
+            al(g.upd_m) && al(g.upd_v) && al(g.upd_shadow) && (lds & 7) == 0;
   }
   const size_t smem = kPairSmem;
   auto kern = gemm_pair_kernel<TO, A_MN, B_MN>;
@@ -543,6 +552,8 @@ bool gemm_pair_eligible(const GemmArgs& g) {
   gemm_tc_splits(g, &single_steps);
   return pair_steps < single_steps;
 }
+
+int gemm_pair_split_count(const GemmArgs& g) { return pair_splits(g, nullptr); }
 
 cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s) {
   if (g.a_mn) return launch_pair<float, true, true>(g, err, s);    // dW (fp32 out)

@@ -39,6 +39,22 @@ struct GemmArgs {
   // null: each split writes its partial tile there and one pass adds the
   // splits in order (deterministic, unlike atomics).
   float* split_ws = nullptr; size_t split_ws_floats = 0;
+  // Column partial sums of the stored output (tcgen05 kernels, bf16 outputs,
+  // no split over K), or null: col_part[(m / 32) * N + n] = sum of the stored
+  // out[m', n] over the rows m' of the 32-row group of m, fixed order.  The
+  // bias gradient of the layer whose output gradient this GEMM writes is then
+  // the sum of ceil(M / 32) partial rows instead of a pass over out.
+  float* col_part = nullptr;
+  // Adam update of the weight fused into a weight-gradient epilogue
+  // (tcgen05 kernels, fp32 output, no split over K), or upd_p null: the
+  // parameters, moments and bf16 copy have out's layout; upd_scal points to
+  // {lr / (1 - b1^t), 1 / sqrt(1 - b2^t)} in device memory.
+  float* upd_p = nullptr;
+  float* upd_m = nullptr;
+  float* upd_v = nullptr;
+  void* upd_shadow = nullptr;      // bf16
+  const float* upd_scal = nullptr;
+  float upd_b1 = 0.f, upd_b2 = 0.f, upd_eps = 0.f;
 };
 
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
@@ -59,6 +75,8 @@ int gemm_tc_splits(const GemmArgs& g, double* steps);
 // as well.
 bool gemm_pair_eligible(const GemmArgs& g);
 cudaError_t gemm_pair(const GemmArgs& g, int* err, cudaStream_t s);
+// Split count over K the SM-pair kernel picks for g.
+int gemm_pair_split_count(const GemmArgs& g);
 
 // ---- loss ------------------------------------------------------------------
 // Softmax cross-entropy from logits whose per-row softmax partials the head
@@ -84,6 +102,9 @@ cudaError_t mse_loss(DType t, const void* o, const void* target, size_t n, void*
 // out[n] = sum over rows of src[r, n]  (fp32 result), deterministic two passes.
 cudaError_t colsum(DType t, const void* src, int rows, int cols, long long ld, float* partials,
                    size_t partial_floats, float* out, cudaStream_t s);
+// out[n] = sum over r < chunks of partials[r * cols + n] (fixed order).
+cudaError_t colsum_partials(const float* partials, int chunks, int cols, float* out,
+                            cudaStream_t s);
 // Target block count of colsum's first pass (about two per SM); a partials
 // buffer of kColsumBlocks * 2048 floats lets it reach that for any width.
 constexpr int kColsumBlocks = 2 * 152;
@@ -122,7 +143,7 @@ struct Chunk {  // a run of one tensor's elements in the flat buffers
 cudaError_t adam_update(const Chunk* chunks, int n_chunks, float* p, const float* g, float* m,
                         float* v, void* shadow, float lr_over_bc1, float inv_sqrt_bc2,
                         float beta1, float beta2, float eps, cudaStream_t s);
-// The optimizer update kernels' argument layout, for replaying a captured
+// The optimizer update kernels' (and write_step_scalars') argument layout, for replaying a captured
 // step with new step scalars: argument count and sizes, and the indices of
 // lr / (1 - b1^t), 1 / sqrt(1 - b2^t) (Adam, LaProp) or lr (SGD, momentum).
 struct OptKernelInfo {
@@ -138,6 +159,9 @@ cudaError_t momentum_update(const Chunk* chunks, int n_chunks, float* p, const f
                             void* shadow, float lr, float mu, cudaStream_t s);
 cudaError_t sgd_update(const Chunk* chunks, int n_chunks, float* p, const float* g, void* shadow,
                        float lr, cudaStream_t s);
+// dst[0] = lr_bc1, dst[1] = inv_sqrt_bc2 (the step scalars a fused update
+// reads; a one-thread kernel, so that a replayed step graph can patch them).
+cudaError_t write_step_scalars(float* dst, float lr_bc1, float inv_sqrt_bc2, cudaStream_t s);
 cudaError_t cast_shadow(const Chunk* chunks, int n_chunks, const float* p, void* shadow,
                         cudaStream_t s);
 

@@ -323,6 +323,14 @@ cudaError_t colsum(DType t, const void* src, int rows, int cols, long long ld, f
   return cudaGetLastError();
 }
 
+cudaError_t colsum_partials(const float* partials, int chunks, int cols, float* out,
+                            cudaStream_t s) {
+  if (cols <= 0) return cudaSuccess;
+  if (chunks <= 0) return cudaErrorInvalidValue;
+  colsum_pass2_wide<<<(cols + 31) / 32, 256, 0, s>>>(partials, chunks, cols, out);
+  return cudaGetLastError();
+}
+
 cudaError_t rmsnorm_fwd(DType t, const void* x, const float* gamma, void* y, float* rstd, int rows,
                         int d, float eps, cudaStream_t s) {
   if (d > NORM_THREADS * NORM_MAX_PER_THREAD) return cudaErrorInvalidValue;

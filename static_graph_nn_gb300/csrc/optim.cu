@@ -18,11 +18,9 @@
 namespace mg {
 namespace {
 
-__device__ __forceinline__ void adam_one(float& p, float g, float& m, float& v, float lr_bc1,
-                                         float inv_sqrt_bc2, float b1, float b2, float eps) {
-  m = b1 * m + (1.0f - b1) * g;
-  v = b2 * v + (1.0f - b2) * g * g;
-  p -= lr_bc1 * m / (sqrtf(v) * inv_sqrt_bc2 + eps);
+__global__ void step_scalars_kernel(float* dst, float lr_bc1, float inv_sqrt_bc2) {
+  dst[0] = lr_bc1;
+  dst[1] = inv_sqrt_bc2;
 }
 
 __global__ void __launch_bounds__(256) adam_kernel(const Chunk* chunks, float* p, const float* g,
@@ -177,11 +175,17 @@ __global__ void nonfinite_kernel(const float* d, size_t n, unsigned long long* f
 
 }  // namespace
 
+cudaError_t write_step_scalars(float* dst, float lr_bc1, float inv_sqrt_bc2, cudaStream_t s) {
+  step_scalars_kernel<<<1, 1, 0, s>>>(dst, lr_bc1, inv_sqrt_bc2);
+  return cudaGetLastError();
+}
+
 bool optimizer_kernel_info(const void* func, OptKernelInfo* info) {
   // argument lists of the update kernels above: pointers are 8 bytes, scalars 4
   static const int two_moment[11] = {8, 8, 8, 8, 8, 8, 4, 4, 4, 4, 4};
   static const int momentum[7] = {8, 8, 8, 8, 8, 4, 4};
   static const int sgd[5] = {8, 8, 8, 8, 4};
+  static const int scalars[3] = {8, 4, 4};
   const int* sizes = nullptr;
   if (func == reinterpret_cast<const void*>(adam_kernel) ||
       func == reinterpret_cast<const void*>(laprop_kernel)) {
@@ -189,6 +193,12 @@ bool optimizer_kernel_info(const void* func, OptKernelInfo* info) {
     info->nargs = 11;
     info->i_lr_bc1 = 6;
     info->i_inv_sqrt_bc2 = 7;
+    info->i_lr = -1;
+  } else if (func == reinterpret_cast<const void*>(step_scalars_kernel)) {
+    sizes = scalars;
+    info->nargs = 3;
+    info->i_lr_bc1 = 1;
+    info->i_inv_sqrt_bc2 = 2;
     info->i_lr = -1;
   } else if (func == reinterpret_cast<const void*>(momentum_kernel)) {
     sizes = momentum;

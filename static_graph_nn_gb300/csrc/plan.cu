@@ -62,6 +62,15 @@ struct Node {
   // linear
   int d_in = 0, d_out = 0, has_bias = 0, act = 0, skip = -1, z = -1;
   size_t w_off = 0, b_off = 0;
+  // bf16 linear with a bias whose output feeds a linear: workspace offset of
+  // the [ceil(batch / 32), d_out] column partials of its output gradient,
+  // written by the consumer's input-gradient GEMM (0: none)
+  size_t cp_off = 0;
+  // bf16 linear under Adam whose weight gradient runs on the tensor cores
+  // without a split over K: the weight's update is fused into that GEMM's
+  // epilogue, so its input gradient (the last reader of the bf16 weight copy)
+  // is formed first
+  bool fuse_upd = false;
   // rmsnorm
   int d = 0;
   float eps = 0.f;
@@ -104,6 +113,13 @@ struct mg_plan {
   size_t shadow_off = 0, chunks_off = 0, loss_off = 0, rowloss_off = 0, partial_off = 0,
          colsum_off = 0, flag_off = 0, lse_part_off = 0;
   size_t split_off = 0, split_floats = 0;   // strict weight gradients split over K
+  size_t scal_off = 0;       // Adam's step scalars for fused updates (2 floats)
+  // MG_FUSED_UPDATE=1: Adam's weight updates in the weight-gradient GEMMs'
+  // epilogues where they can be (measured slower on GB300 for the large
+  // MLPs: the epilogue's extra 26 bytes per weight outlast the next tile's
+  // main loop and stall the tensor pipe), else all in the optimizer kernels
+  bool fuse_update = false;
+  bool any_fused = false;    // some node's update is fused into its weight-gradient GEMM
   int lse_parts = 0;         // 128-column softmax partials per logits row (0: not planned)
   int n_chunks = 0;
   const float* last_params = nullptr;
@@ -208,6 +224,9 @@ struct Exec {
   float lr = 0.f;
   int step = 1;
   bool ce_parts = false;   // the head GEMM wrote the logits' softmax partials
+  // per node: its output gradient's column partials were written by the
+  // consumer's input-gradient GEMM in this backward (bias gradient = their sum)
+  std::vector<unsigned char> db_parts;
 };
 
 template <class F>
@@ -261,6 +280,7 @@ double gemm_bytes(const GemmArgs& g) {
   if (g.out_z) b += aux * g.M * g.N;
   if (g.dact) b += aux * g.M * g.N;
   if (g.resid) b += aux * g.M * g.N;
+  if (g.col_part) b += 4.0 * ((g.M + 31) / 32) * g.N;
   return b;
 }
 
@@ -384,15 +404,26 @@ void loss_pass(Exec& e, const void* labels) {
   }
 }
 
+// Adam's and LaProp's step scalars: lr / (1 - b1^t) and 1 / sqrt(1 - b2^t).
+void step_scalars(const mg_plan* p, float lr, int step, float* lr_bc1, float* inv_sqrt_bc2) {
+  double bc1 = 1.0 - std::pow((double)p->beta1, (double)step);
+  double bc2 = 1.0 - std::pow((double)p->beta2, (double)step);
+  *lr_bc1 = (float)(lr / bc1);
+  *inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+}
+
 // Optimizer update of node ni's parameters, on the auxiliary stream once the
-// node's backward kernels (the last readers of its weights) have run.
-void node_update(Exec& e, int ni) {
+// node's backward kernels (the last readers of its weights) have run; with
+// skip_weight, only its tensors after the weight (the weight's update was
+// fused into its gradient GEMM).
+void node_update(Exec& e, int ni, bool skip_weight = false) {
   mg_plan* p = e.p;
   const Node& n = p->nodes[ni];
-  if (n.nt == 0) return;
-  const int c0 = p->tensor_chunk[n.t0], c1 = p->tensor_chunk[n.t0 + n.nt];
+  const int t_lo = n.t0 + (skip_weight ? 1 : 0), t_hi = n.t0 + n.nt;
+  if (t_lo >= t_hi) return;
+  const int c0 = p->tensor_chunk[t_lo], c1 = p->tensor_chunk[t_hi];
   double np = 0;
-  for (int t = n.t0; t < n.t0 + n.nt; ++t) np += (double)p->p_rows[t] * p->p_cols[t];
+  for (int t = t_lo; t < t_hi; ++t) np += (double)p->p_rows[t] * p->p_cols[t];
   const Chunk* chunks = wsp<Chunk>(p, p->chunks_off) + c0;
   void* shadow = p->dt == DT_BF16 ? p->ws + p->shadow_off : nullptr;
   if (!e.dry && e.err == cudaSuccess) {
@@ -402,9 +433,8 @@ void node_update(Exec& e, int ni) {
   }
   char nm[96];
   if (p->optimizer == MG_OPT_ADAM || p->optimizer == MG_OPT_LAPROP) {
-    double bc1 = 1.0 - std::pow((double)p->beta1, (double)e.step);
-    double bc2 = 1.0 - std::pow((double)p->beta2, (double)e.step);
-    float lr_bc1 = (float)(e.lr / bc1), inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+    float lr_bc1, inv_sqrt_bc2;
+    step_scalars(p, e.lr, e.step, &lr_bc1, &inv_sqrt_bc2);
     const bool lap = p->optimizer == MG_OPT_LAPROP;
     snprintf(nm, sizeof nm, "%s[l%d] %.0f params", lap ? "laprop" : "adam", n.layer, np);
     site_on(e, p->aux, nm, 0, np * (28.0 + (shadow ? 2.0 : 0.0)), 1, [&] {
@@ -426,11 +456,49 @@ void node_update(Exec& e, int ni) {
   }
 }
 
+// dW = X^T dZ of linear node n   (M = d_in, N = d_out, K = batch)
+GemmArgs dw_args(mg_plan* p, const Node& n, float* grads, const void* x) {
+  GemmArgs g;
+  g.M = n.d_in; g.N = n.d_out; g.K = p->batch;
+  g.A = val_ptr(p, n.in, x); g.lda = n.d_in; g.a_mn = 1;
+  g.B = grad_ptr(p, n.out); g.ldb = n.d_out; g.b_k = 0;
+  g.in_type = p->dt; g.aux_type = p->dt;
+  g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
+  if (p->split_floats) {
+    g.split_ws = wsp<float>(p, p->split_off);
+    g.split_ws_floats = p->split_floats;
+  }
+  return g;
+}
+
+// Whether the weight update of a node with these weight-gradient arguments
+// can run in the GEMM's epilogue: Adam, bf16, a tensor-core kernel and no
+// split over K (a split's partial tiles are not the gradient).
+bool update_fusable(mg_plan* p, const GemmArgs& g) {
+  if (!p->fuse_update || p->dt != DT_BF16 || p->optimizer != MG_OPT_ADAM || !tc_path(p, g))
+    return false;
+  return (pair_path(p, g) ? gemm_pair_split_count(g) : gemm_tc_splits(g, nullptr)) == 1;
+}
+
+// Plan-time choice of the fused updates (the input pointer is taken as
+// aligned; a step whose input is not falls back to the optimizer kernel).
+void plan_fused_updates(mg_plan* p) {
+  p->any_fused = false;
+  for (Node& n : p->nodes) {
+    n.fuse_upd = false;
+    if (n.kind != NK_LINEAR || !p->values[n.out].need_grad) continue;
+    n.fuse_upd = update_fusable(p, dw_args(p, n, nullptr, nullptr));
+    p->any_fused = p->any_fused || n.fuse_upd;
+  }
+}
+
 void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
   mg_plan* p = e.p;
+  e.db_parts.assign(p->nodes.size(), 0);
   const DType dt = p->dt;
   const void* wbase = dt == DT_BF16 ? (const void*)(p->ws + p->shadow_off) : (const void*)params;
   GemmArgs deferred;   // the deferred node's weight gradient
+  bool deferred_fused = false;
   for (int ni = (int)p->nodes.size() - 1; ni >= 0; --ni) {
     const Node& n = p->nodes[ni];
     if (!p->values[n.out].need_grad) continue;
@@ -438,39 +506,60 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
     const Value& vin = p->values[n.in];
     const void* dadd = vin.pending_add >= 0 ? grad_ptr(p, vin.pending_add) : nullptr;
     if (n.kind == NK_LINEAR) {
-      // dW = X^T dZ   (M = d_in, N = d_out, K = batch)
-      GemmArgs g;
-      g.M = n.d_in; g.N = n.d_out; g.K = p->batch;
-      g.A = val_ptr(p, n.in, x); g.lda = n.d_in; g.a_mn = 1;
-      g.B = gy; g.ldb = n.d_out; g.b_k = 0;
-      g.in_type = dt; g.aux_type = dt;
-      g.out = grads + n.w_off; g.ldo = n.d_out; g.out_type = DT_F32;
-      if (p->split_floats) {
-        g.split_ws = wsp<float>(p, p->split_off);
-        g.split_ws_floats = p->split_floats;
+      GemmArgs g = dw_args(p, n, grads, x);
+      // the weight's Adam step in the dW epilogue (Adam's state as the
+      // optimizer kernel would leave it)
+      const bool fused = n.fuse_upd && update_fusable(p, g);
+      if (fused && !e.dry) {
+        g.upd_p = e.params + n.w_off;
+        g.upd_m = e.m + n.w_off;
+        g.upd_v = e.v + n.w_off;
+        g.upd_shadow = p->ws + p->shadow_off + n.w_off * 2;
+        g.upd_scal = wsp<float>(p, p->scal_off);
+        g.upd_b1 = p->beta1;
+        g.upd_b2 = p->beta2;
+        g.upd_eps = p->adam_eps;
       }
       if (n.has_bias) {
         // db = column sums of dZ, on the auxiliary stream (only the optimizer
-        // reads it), overlapping this node's dW and dX products
+        // reads it), overlapping this node's dW and dX products: the sum of
+        // the column partials the consumer's input-gradient GEMM wrote, else
+        // a pass over dZ
         if (!e.dry && e.err == cudaSuccess) {
           cudaError_t r = cudaEventRecord(p->node_ev[2 * ni + 1], e.s);
           if (r == cudaSuccess) r = cudaStreamWaitEvent(p->aux, p->node_ev[2 * ni + 1], 0);
           if (r != cudaSuccess) e.err = r;
         }
         char nm[96];
-        snprintf(nm, sizeof nm, "db_colsum[l%d] %dx%d", n.layer, p->batch, n.d_out);
-        site_on(e, p->aux, nm, 0, (double)dtype_size(dt) * p->batch * n.d_out + 4.0 * n.d_out, 2,
-                [&] {
-                  return colsum(dt, gy, p->batch, n.d_out, n.d_out, wsp<float>(p, p->colsum_off),
-                                kColsumFloats, grads + n.b_off, p->aux);
-                });
+        if (e.db_parts[ni]) {
+          const int chunks = (p->batch + 31) / 32;
+          snprintf(nm, sizeof nm, "db_parts[l%d] %dx%d", n.layer, chunks, n.d_out);
+          site_on(e, p->aux, nm, 0, 4.0 * chunks * n.d_out + 4.0 * n.d_out, 1, [&] {
+            return colsum_partials(wsp<float>(p, n.cp_off), chunks, n.d_out, grads + n.b_off,
+                                   p->aux);
+          });
+        } else {
+          snprintf(nm, sizeof nm, "db_colsum[l%d] %dx%d", n.layer, p->batch, n.d_out);
+          site_on(e, p->aux, nm, 0, (double)dtype_size(dt) * p->batch * n.d_out + 4.0 * n.d_out,
+                  2, [&] {
+                    return colsum(dt, gy, p->batch, n.d_out, n.d_out,
+                                  wsp<float>(p, p->colsum_off), kColsumFloats, grads + n.b_off,
+                                  p->aux);
+                  });
+        }
       }
-      if (ni == p->defer_dw) {
-        deferred = g;
-      } else {
-        site(e, gemm_name(p, "dW", n.layer, g), 2.0 * g.M * g.N * g.K, gemm_bytes(g), 1,
-             [&] { return run_gemm(p, g, e.s); });
-      }
+      auto weight_grad = [&] {
+        if (ni == p->defer_dw) {
+          deferred = g;
+          deferred_fused = fused;
+        } else {
+          // a fused update reads p, m, v and writes them and the bf16 copy
+          site(e, gemm_name(p, fused ? "dW+adam" : "dW", n.layer, g), 2.0 * g.M * g.N * g.K,
+               gemm_bytes(g) + (fused ? 26.0 * g.M * g.N : 0.0), 1,
+               [&] { return run_gemm(p, g, e.s); });
+        }
+      };
+      if (!n.fuse_upd) weight_grad();
       if (vin.need_grad) {
         // dX = dZ W^T, times act'(saved) of the producer of X, plus the skip gradient
         GemmArgs h;
@@ -502,10 +591,17 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
         }
         if (dadd) { h.resid = dadd; h.ldr = n.d_in; }
         h.out = grad_ptr(p, n.in); h.ldo = n.d_in; h.out_type = dt;
+        if (vin.producer >= 0 && p->nodes[vin.producer].cp_off && tc_path(p, h)) {
+          // this GEMM writes the producer's whole output gradient: its
+          // epilogue also leaves the column partials of the producer's db
+          h.col_part = wsp<float>(p, p->nodes[vin.producer].cp_off);
+          e.db_parts[vin.producer] = 1;
+        }
         site(e, gemm_name(p, "dX", n.layer, h), 2.0 * h.M * h.N * h.K, gemm_bytes(h), 1,
              [&] { return run_gemm(p, h, e.s); });
       }
-      if (ni != p->defer_dw) node_update(e, ni);
+      if (n.fuse_upd) weight_grad();   // after dX, the last reader of the bf16 weights
+      if (ni != p->defer_dw) node_update(e, ni, fused);
     } else if (n.kind == NK_RMSNORM) {
       void* dx = vin.need_grad ? grad_ptr(p, n.in) : nullptr;
       double bytes = (double)dtype_size(dt) * p->batch * n.d * (dx ? (dadd ? 4 : 3) : 2);
@@ -544,9 +640,11 @@ void backward_pass(Exec& e, const float* params, float* grads, const void* x) {
   }
   if (p->defer_dw >= 0) {
     const Node& n = p->nodes[p->defer_dw];
-    site(e, gemm_name(p, "dW", n.layer, deferred), 2.0 * deferred.M * deferred.N * deferred.K,
-         gemm_bytes(deferred), 1, [&] { return run_gemm(p, deferred, e.s); });
-    node_update(e, p->defer_dw);
+    site(e, gemm_name(p, deferred_fused ? "dW+adam" : "dW", n.layer, deferred),
+         2.0 * deferred.M * deferred.N * deferred.K,
+         gemm_bytes(deferred) + (deferred_fused ? 26.0 * deferred.M * deferred.N : 0.0), 1,
+         [&] { return run_gemm(p, deferred, e.s); });
+    node_update(e, p->defer_dw, deferred_fused);
   }
 }
 
@@ -568,6 +666,15 @@ void train_schedule(Exec& e, float* params, float* grads, float* m, float* v, co
   e.v = v;
   e.lr = lr;
   e.step = step;
+  mg_plan* p = e.p;
+  if (p->any_fused) {
+    // Adam's step scalars in device memory for the fused updates (a kernel
+    // node, so that a replayed graph carries each step's values)
+    float lr_bc1, inv;
+    step_scalars(p, lr, step, &lr_bc1, &inv);
+    site(e, "step_scalars", 0, 8, 1,
+         [&] { return write_step_scalars(wsp<float>(p, p->scal_off), lr_bc1, inv, e.s); });
+  }
   forward_pass(e, params, x);
   loss_pass(e, labels);
   backward_pass(e, params, grads, x);
@@ -879,6 +986,16 @@ void layout_workspace(mg_plan* p) {
       n.dsum_off = b.take(B * n.nh * 4);
     }
   }
+  // bias-gradient column partials, one buffer per layer: the optimizer
+  // stream sums a layer's partials while the main stream goes on to write the
+  // next layer's
+  if (p->dt == DT_BF16 && p->use_tc) {
+    for (Node& n : p->nodes) {
+      if (n.kind != NK_LINEAR || !n.has_bias || !p->values[n.out].need_grad) continue;
+      for (const Node& c : p->nodes)
+        if (c.in == n.out && c.kind == NK_LINEAR) n.cp_off = b.take((B + 31) / 32 * n.d_out * 4);
+    }
+  }
   if (p->dt == DT_BF16) p->shadow_off = b.take(p->n_params * 2);
   // chunks
   p->n_chunks = 0;
@@ -888,6 +1005,7 @@ void layout_workspace(mg_plan* p) {
   }
   p->chunks_off = b.take(sizeof(Chunk) * (size_t)p->n_chunks);
   p->loss_off = b.take(16);
+  p->scal_off = b.take(16);
   p->flag_off = b.take(16);
   p->rowloss_off = b.take(B * 4);
   size_t part = 0;
@@ -952,6 +1070,12 @@ void build_dump(mg_plan* p) {
            p->grad_bytes, p->grad_bytes_unaliased, p->alias ? "" : "; MG_NO_ALIAS set");
   s += b;
   if (p->recompute_gelu) s += "  GELU pre-activations: recomputed in the backward (MG_RECOMPUTE_GELU set)\n";
+  for (const Node& n : p->nodes)
+    if (n.fuse_upd) {
+      snprintf(b, sizeof b, "  layer %d: Adam update of the weight fused into its gradient GEMM\n", n.layer);
+      s += b;
+    }
+  if (p->fuse_update && !p->any_fused) s += "  MG_FUSED_UPDATE set: no weight update qualifies\n";
   for (size_t i = 0; i < p->p_off.size(); ++i) {
     snprintf(b, sizeof b, "  param %zu: offset %zu [%d x %d]\n", i, p->p_off[i], p->p_rows[i],
              p->p_cols[i]);
@@ -997,14 +1121,6 @@ void drop_graph(mg_plan::StepGraph& g) {
   g.gexec = nullptr;
   g.graph = nullptr;
   g.opt_nodes.clear();
-}
-
-// The optimizer's step scalars as node_update computes them.
-void step_scalars(const mg_plan* p, float lr, int step, float* lr_bc1, float* inv_sqrt_bc2) {
-  double bc1 = 1.0 - std::pow((double)p->beta1, (double)step);
-  double bc2 = 1.0 - std::pow((double)p->beta2, (double)step);
-  *lr_bc1 = (float)(lr / bc1);
-  *inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
 }
 
 // The graph entry for this buffer set (created, evicting the least recently
@@ -1135,6 +1251,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
   if (const char* ev = getenv("MG_NO_ALIAS")) p->alias = !(ev[0] == '1' && ev[1] == 0);
   if (const char* ev = getenv("MG_RECOMPUTE_GELU")) p->recompute_gelu = ev[0] == '1' && ev[1] == 0;
   if (const char* ev = getenv("MG_GRAPH")) p->use_graph = !(ev[0] == '0' && ev[1] == 0);
+  if (const char* ev = getenv("MG_FUSED_UPDATE")) p->fuse_update = ev[0] == '1' && ev[1] == 0;
   layout_workspace(p);
   e = cudaMalloc((void**)&p->ws, p->ws_bytes);
   if (e != cudaSuccess) {
@@ -1166,6 +1283,7 @@ mg_status mg_step_plan_create(const mg_graph_desc* desc, mg_plan** out) {
     delete p;
     return r;
   }
+  plan_fused_updates(p);
   // register the schedule's kernels (dry run: no launches)
   Exec ex{p, nullptr, true, false};
   train_schedule(ex, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, 1);
