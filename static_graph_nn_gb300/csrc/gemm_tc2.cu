@@ -62,9 +62,15 @@ __device__ __forceinline__ uint32_t map_to(const void* p, uint32_t rank) {
   return out;
 }
 
+// Arrive on a barrier of another CTA of the cluster.  Default semantics
+// (release at CTA scope): it signals that this thread's TMEM reads are done
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync), and must not
+// wait for the thread's global stores to reach cluster scope -- nothing the
+// waiting MMA thread reads depends on them.  (With .release.cluster each
+// epilogue warp stalled on a memory barrier per tile, holding the
+// accumulator until its output stores were acknowledged.)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on the
@@ -358,10 +364,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       const int m = m0 + row_in_tile;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * P_BN);
       float pm = -INFINITY, ps = 0.0f;             // softmax partial of this row's 128 columns
-#pragma unroll 1
-      for (int c = half * (P_BN / 64); c < (half + 1) * (P_BN / 64); ++c) {
+      auto chunk = [&](int c, uint32_t (&r)[32]) {
         float v[32];
-        tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         if (m < P.g.M && n0 + c * 32 < P.g.N) {
           if (P.splits > 1) {
             split_add32(P.g, P.vec != 0, m, n0 + c * 32, v);
@@ -374,11 +380,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         // warp-uniform: the warp's 32-row group starts below M, the chunk below N
         if (P.g.col_part && (m & ~31) < P.g.M && n0 + c * 32 < P.g.N)
           col_partial32<TO>(P.g, m, n0 + c * 32, lane, v);
+      };
+      // two pairs of 32-column chunks; the second pair's TMEM loads are this
+      // warp's last reads of the accumulator, which is released to the MMA
+      // thread before that pair's epilogue (loads, math, stores) runs
+#pragma unroll 1
+      for (int cp = 0; cp < 2; ++cp) {
+        const int c0 = half * (P_BN / 64) + 2 * cp;
+        uint32_t r0[32], r1[32];
+        tmem_ld32_async(taddr + c0 * 32, r0);
+        tmem_ld32_async(taddr + (c0 + 1) * 32, r1);
+        tmem_wait_regs(r0);
+        reg_fence(r1);
+        if (cp == 1) {
+          tc_fence_before();
+          mbar_arrive_remote(leader_tempty[acc]);
+        }
+        chunk(c0, r0);
+        chunk(c0 + 1, r1);
       }
       if (P.g.lse_part && m < P.g.M && n0 + half * (P_BN / 2) < P.g.N)
         P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (P_BN / 2)) / 128] = make_float2(pm, ps);
-      tc_fence_before();
-      mbar_arrive_remote(leader_tempty[acc]);
     }
   }
 

@@ -2,7 +2,7 @@
 // Contents section: SGD and Adam; Adam moments exist only when requested).
 //
 // One launch updates every tensor: a chunk table lists runs of at most
-// kChunk elements of one tensor, one block per chunk, float4 accesses.  The
+// 2048 elements of one tensor, one block per chunk, float4 accesses.  The
 // same pass writes the bf16 copy of each updated weight for the next forward.
 //
 // Adam (t = step, 1-based): m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2,
