@@ -112,6 +112,44 @@ __device__ __forceinline__ void softmax_partial32(const GemmArgs& g, int n0, con
   ps += acc;
 }
 
+// 32 bytes in one store (a full L2 sector per lane): 16 floats as bf16, or 8
+// floats; p 32-byte aligned.
+__device__ __forceinline__ void st32b(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void st16bf(bf16* p, const float* f) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  st32b(p, w);
+}
+__device__ __forceinline__ void st8f32(float* p, const float* f) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(f[i]);
+  st32b(p, w);
+}
+
+// 16 bf16 values from one 32-byte load (p 32-byte aligned), widened.
+__device__ __forceinline__ void ld16bf(const bf16* p, float* f) {
+  uint32_t w[8];
+  asm("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
 // Column sums over a warp's 32 rows: lane l holds row l's 32 consecutive
 // columns in x; returns the sum of column l over the 32 lanes.  A butterfly
 // reduce-scatter: at each of five steps every lane keeps one half of its

@@ -39,6 +39,7 @@ struct TcParams {
   int tiles_m, tiles_n, k_blocks;
   int splits, kb_per;                  // split-K: K blocks [s*kb_per, (s+1)*kb_per) per split
   int vec;                             // epilogue pointers/strides allow 16-byte vectors
+  int vec32;                           // out, out_z, saved and resid rows allow 32-byte accesses
   int* err;                            // set to 1 on a timed-out wait
 };
 
@@ -74,8 +75,8 @@ __device__ __forceinline__ void store8_bf16(bf16* p, const float* f) {
 // On return v holds the values stored (before their rounding to TO) at the
 // columns below N.
 template <typename TO>
-__device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int m, int n0,
-                                               float (&v)[32]) {
+__device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, bool vec32, int m,
+                                               int n0, float (&v)[32]) {
   const bool full = vec && n0 + 32 <= g.N;
   if (full) {
     if (g.bias) {
@@ -93,7 +94,13 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int 
     if (g.out_z) {
       bf16* z = static_cast<bf16*>(g.out_z) + (size_t)m * g.ldz + n0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) store8_bf16(z + 8 * q, v + 8 * q);
+      if (vec32) {
+        st16bf(z, v);
+        st16bf(z + 16, v + 16);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) store8_bf16(z + 8 * q, v + 8 * q);
+      }
     }
     if (g.act) {
 #pragma unroll
@@ -102,26 +109,44 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& g, bool vec, int 
     if (g.dact) {
       const bf16* sv = static_cast<const bf16*>(g.saved) + (size_t)m * g.lds + n0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float f[8];
-        load8_bf16(sv + 8 * q, f);
+      for (int q = 0; q < 2; ++q) {
+        float f[16];
+        if (vec32) {
+          ld16bf(sv + 16 * q, f);
+        } else {
+          load8_bf16(sv + 16 * q, f);
+          load8_bf16(sv + 16 * q + 8, f + 8);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          v[8 * q + i] = round_value_tc<TO>(v[8 * q + i]) * act_grad_from_saved(g.dact, f[i]);
+        for (int i = 0; i < 16; ++i)
+          v[16 * q + i] = round_value_tc<TO>(v[16 * q + i]) * act_grad_from_saved(g.dact, f[i]);
       }
     }
     if (g.resid) {
       const bf16* rv = static_cast<const bf16*>(g.resid) + (size_t)m * g.ldr + n0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float f[8];
-        load8_bf16(rv + 8 * q, f);
+      for (int q = 0; q < 2; ++q) {
+        float f[16];
+        if (vec32) {
+          ld16bf(rv + 16 * q, f);
+        } else {
+          load8_bf16(rv + 16 * q, f);
+          load8_bf16(rv + 16 * q + 8, f + 8);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * q + i] += f[i];
+        for (int i = 0; i < 16; ++i) v[16 * q + i] += f[i];
       }
     }
     TO* out = static_cast<TO*>(g.out) + (size_t)m * g.ldo + n0;
-    if (sizeof(TO) == 2) {
+    if (vec32) {
+      if (sizeof(TO) == 2) {
+        st16bf(reinterpret_cast<bf16*>(out), v);
+        st16bf(reinterpret_cast<bf16*>(out) + 16, v + 16);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8f32(reinterpret_cast<float*>(out) + 8 * q, v + 8 * q);
+      }
+    } else if (sizeof(TO) == 2) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) store8_bf16(reinterpret_cast<bf16*>(out) + 8 * q, v + 8 * q);
     } else {
@@ -304,27 +329,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       static_assert(BN == 256, "softmax partials cover 128 columns per epilogue warp");
       float pm = -INFINITY, ps = 0.0f;             // softmax partial of this row's 128 columns
-#pragma unroll 1
-      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+      auto chunk = [&](int c, uint32_t (&r)[32]) {
         float v[32];
-        tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         if (m < P.g.M && n0 + c * 32 < P.g.N) {
           if (P.splits > 1) {
             split_add_row32(P.g, P.vec != 0, m, n0 + c * 32, v);
           } else {
             if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
-            epilogue_row32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+            epilogue_row32<TO>(P.g, P.vec != 0, P.vec32 != 0, m, n0 + c * 32, v);
             if (sizeof(TO) == 4 && P.g.upd_p) adam_update32(P.g, P.vec != 0, m, n0 + c * 32, v);
           }
         }
         // warp-uniform: the warp's 32-row group starts below M, the chunk below N
         if (P.g.col_part && (m & ~31) < P.g.M && n0 + c * 32 < P.g.N)
           col_partial32<TO>(P.g, m, n0 + c * 32, lane, v);
+      };
+      // two pairs of 32-column chunks; the accumulator is released to the MMA
+      // thread once the second pair is in registers, before its epilogue runs
+#pragma unroll 1
+      for (int cp = 0; cp < 2; ++cp) {
+        const int c0 = half * (BN / 64) + 2 * cp;
+        uint32_t r0[32], r1[32];
+        tmem_ld32_async(taddr + c0 * 32, r0);
+        tmem_ld32_async(taddr + (c0 + 1) * 32, r1);
+        tmem_wait_regs(r0);
+        reg_fence(r1);
+        if (cp == 1) {
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
+        chunk(c0, r0);
+        chunk(c0 + 1, r1);
       }
       if (P.g.lse_part && m < P.g.M && n0 + half * (BN / 2) < P.g.N)
         P.g.lse_part[(size_t)m * P.g.lse_ld + (n0 + half * (BN / 2)) / 128] = make_float2(pm, ps);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
     }
   }
 
@@ -407,6 +447,11 @@ cudaError_t launch_tc(const GemmArgs& g, int* err, cudaStream_t s) {
     const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
     P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) &&
             al(g.upd_p) && al(g.upd_m) && al(g.upd_v) && al(g.upd_shadow) && (lds & 7) == 0;
+    auto al32 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    const long long out_elems32 = g.out_type == DT_F32 ? 8 : 16;   // elements per 32 bytes
+    P.vec32 = P.vec && al32(g.out) && al32(g.out_z) && al32(g.saved) && al32(g.resid) &&
+              g.ldo % out_elems32 == 0 && (g.out_z == nullptr || g.ldz % 16 == 0) &&
+              (g.saved == nullptr || g.lds % 16 == 0) && (g.resid == nullptr || g.ldr % 16 == 0);
   }
   const size_t smem = 1024 + (size_t)STAGES * (TC_BM + BN) * TC_BK * 2 + (2 * STAGES + 4) * 8 + 16;
   auto kern = gemm_tc_kernel<BN, STAGES, TO, A_MN, B_MN>;

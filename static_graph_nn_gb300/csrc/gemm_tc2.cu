@@ -46,6 +46,7 @@ struct PairParams {
   int tiles_m, tiles_n, k_blocks;   // tiles_m counts 256-row pair tiles
   int splits, kb_per;               // split-K: K blocks [s*kb_per, (s+1)*kb_per) per split
   int vec;
+  int vec32;                        // out, out_z, saved and resid rows allow 32-byte accesses
   int* err;
 };
 
@@ -155,7 +156,8 @@ __device__ __forceinline__ void split_add32(const GemmArgs& g, bool vec, int m, 
 // return v holds the values stored (before their rounding to TO) at the
 // columns below N.
 template <typename TO>
-__device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, int m, int n0, float (&v)[32]) {
+__device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, bool vec32, int m, int n0,
+                                      float (&v)[32]) {
   if (vec && n0 + 32 <= g.N) {
     if (g.bias) {
       const float4* b4 = reinterpret_cast<const float4*>(g.bias + n0);
@@ -171,8 +173,13 @@ __device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, int m, int n0
     }
     if (g.out_z) {
       bf16* z = static_cast<bf16*>(g.out_z) + (size_t)m * g.ldz + n0;
+      if (vec32) {
+        st16bf(z, v);
+        st16bf(z + 16, v + 16);
+      } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) st8f(z + 8 * q, v + 8 * q);
+        for (int q = 0; q < 4; ++q) st8f(z + 8 * q, v + 8 * q);
+      }
     }
     if (g.act) {
 #pragma unroll
@@ -181,25 +188,44 @@ __device__ __forceinline__ void epi32(const GemmArgs& g, bool vec, int m, int n0
     if (g.dact) {
       const bf16* sv = static_cast<const bf16*>(g.saved) + (size_t)m * g.lds + n0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float f[8];
-        ld8f(sv + 8 * q, f);
+      for (int q = 0; q < 2; ++q) {
+        float f[16];
+        if (vec32) {
+          ld16bf(sv + 16 * q, f);
+        } else {
+          ld8f(sv + 16 * q, f);
+          ld8f(sv + 16 * q + 8, f + 8);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * q + i] = rv<TO>(v[8 * q + i]) * act_grad_from_saved(g.dact, f[i]);
+        for (int i = 0; i < 16; ++i)
+          v[16 * q + i] = rv<TO>(v[16 * q + i]) * act_grad_from_saved(g.dact, f[i]);
       }
     }
     if (g.resid) {
       const bf16* rp = static_cast<const bf16*>(g.resid) + (size_t)m * g.ldr + n0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float f[8];
-        ld8f(rp + 8 * q, f);
+      for (int q = 0; q < 2; ++q) {
+        float f[16];
+        if (vec32) {
+          ld16bf(rp + 16 * q, f);
+        } else {
+          ld8f(rp + 16 * q, f);
+          ld8f(rp + 16 * q + 8, f + 8);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * q + i] += f[i];
+        for (int i = 0; i < 16; ++i) v[16 * q + i] += f[i];
       }
     }
     TO* out = static_cast<TO*>(g.out) + (size_t)m * g.ldo + n0;
-    if (sizeof(TO) == 2) {
+    if (vec32) {
+      if (sizeof(TO) == 2) {
+        st16bf(reinterpret_cast<bf16*>(out), v);
+        st16bf(reinterpret_cast<bf16*>(out) + 16, v + 16);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st8f32(reinterpret_cast<float*>(out) + 8 * q, v + 8 * q);
+      }
+    } else if (sizeof(TO) == 2) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) st8f(reinterpret_cast<bf16*>(out) + 8 * q, v + 8 * q);
     } else {
@@ -373,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             split_add32(P.g, P.vec != 0, m, n0 + c * 32, v);
           } else {
             if (P.g.lse_part) softmax_partial32(P.g, n0 + c * 32, v, pm, ps);
-            epi32<TO>(P.g, P.vec != 0, m, n0 + c * 32, v);
+            epi32<TO>(P.g, P.vec != 0, P.vec32 != 0, m, n0 + c * 32, v);
             if (sizeof(TO) == 4 && P.g.upd_p) adam_update32(P.g, P.vec != 0, m, n0 + c * 32, v);
           }
         }
@@ -541,6 +567,11 @@ cudaError_t launch_pair(const GemmArgs& g, int* err, cudaStream_t s) {
     const long long lds = (g.ldz | g.lds | g.ldr | g.ldo);
     P.vec = al(g.bias) && al(g.out_z) && al(g.saved) && al(g.resid) && al(g.out) && al(g.upd_p) &&
             al(g.upd_m) && al(g.upd_v) && al(g.upd_shadow) && (lds & 7) == 0;
+    auto al32 = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+    const long long out_elems32 = g.out_type == DT_F32 ? 8 : 16;   // elements per 32 bytes
+    P.vec32 = P.vec && al32(g.out) && al32(g.out_z) && al32(g.saved) && al32(g.resid) &&
+              g.ldo % out_elems32 == 0 && (g.out_z == nullptr || g.ldz % 16 == 0) &&
+              (g.saved == nullptr || g.lds % 16 == 0) && (g.resid == nullptr || g.ldr % 16 == 0);
   }
   const size_t smem = kPairSmem;
   auto kern = gemm_pair_kernel<TO, A_MN, B_MN>;
