@@ -507,10 +507,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // ============================================================ backward
 // Both backward kernels follow the forward's plan: persistent CTAs over
 // (128-row block, head, sequence) units dealt heaviest first in snake order,
-// warp 8 the TMA producer, warp 9 an event-driven MMA issuer, warps 0-7 the
-// elementwise work (warp w: TMEM lane quarter w & 3, columns 64 (w >> 2) ..
-// +63), S and dP read from TMEM once and released, and the bf16 products P /
-// dS written back into TMEM as the A operand of the accumulating MMAs.
+// warps 0-15 the elementwise work (warp w: TMEM lane quarter w & 3, columns
+// 32 (w >> 2) .. +31), warp 16 the TMA producer, warps 17 and 18 the MMA
+// issuers; S and dP are read from TMEM once and released, and the bf16
+// products P / dS are written back into TMEM as the A operand of the
+// accumulating MMAs.
 constexpr int BWD_NST = 3;   // ring stages of the streamed operand pair
 
 __device__ __forceinline__ bool bwd_unit(int k, int n_units, int hb, int H, int& major, int& h,
