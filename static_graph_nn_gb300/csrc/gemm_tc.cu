@@ -16,7 +16,9 @@
 //               publishes each finished accumulator;
 //   warps 2-9   epilogue: tcgen05.ld of one accumulator row per thread (two
 //               warps per TMEM lane quarter, each taking half the columns),
-//               bias, activation, derivative mask, residual, store to global.
+//               bias, activation, derivative mask, residual, store to global;
+//               the accumulator is released once its last columns are in
+//               registers.
 // Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap
 // the main loop of tile i+1.  Every mbarrier wait is bounded; on expiry the
 // kernel records the failure in an error word and unwinds instead of hanging.

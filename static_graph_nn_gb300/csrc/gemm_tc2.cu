@@ -18,8 +18,10 @@
 //               tcgen05.mma.cta_group::2 (M=256, N=256, K=16); its commits are
 //               multicast to both CTAs (stage free, accumulator full);
 //   warps 2-9   (both CTAs) epilogue on this CTA's 128 accumulator rows, two
-//               warps per TMEM lane quarter splitting the 256 columns, then a
-//               remote arrive on the leader's accumulator-free barrier.
+//               warps per TMEM lane quarter splitting the 256 columns; a
+//               remote arrive on the leader's accumulator-free barrier once
+//               the last TMEM loads are in registers, then the rest of the
+//               epilogue (32-byte global accesses where rows allow them).
 // Every wait is bounded; on expiry the error word is set and the pair unwinds.
 #include <cuda.h>
 
