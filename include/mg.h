@@ -277,8 +277,9 @@ mg_status mg_profile_entry(const mg_plan* plan, int i, char* name, size_t name_c
  * Environment variables section).  Runs a fused multiply-add kernel on every
  * SM of the current device for a few milliseconds, synchronises `stream`,
  * and writes the achieved FP32 TFLOP/s (2 flop per FFMA) to *tflops and the
- * FFMA flop per clock per SM to *flop_per_clk_per_sm (may be NULL).  It
- * allocates and frees a few bytes of device memory. */
+ * same rate in flop per SM per clock of the device's maximum SM clock to
+ * *flop_per_clk_per_sm (may be NULL; 0 if the clock rate is not reported).
+ * It allocates and frees a few bytes of device memory. */
 mg_status mg_ffma_peak(double* tflops, double* flop_per_clk_per_sm, mg_stream_t stream);
 
 /* ---- softmax cross-entropy without device allocation -----------------

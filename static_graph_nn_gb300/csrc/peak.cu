@@ -1,7 +1,8 @@
 // Measured FP32 FFMA rate of this GPU: the denominator of the strict-f32
 // path's roofline (its GEMMs are FFMA-only, no tensor cores).  A kernel with
-// eight independent fused multiply-add chains per thread on every SM, timed
-// with CUDA events; nothing of the training step runs here.
+// eight independent fused multiply-add chains per thread, two 1024-thread
+// blocks per SM in the grid, timed with CUDA events; nothing of the training
+// step runs here.
 #include <cstdio>
 
 #include "../../include/mg.h"
@@ -14,24 +15,18 @@ namespace {
 constexpr int kPeakThreads = 1024;
 constexpr int kPeakChains = 8;
 
-__global__ void __launch_bounds__(kPeakThreads) ffma_peak_kernel(float* sink, int iters,
-                                                                 long long* cycles) {
+__global__ void __launch_bounds__(kPeakThreads) ffma_peak_kernel(float* sink, int iters) {
   float a[kPeakChains];
 #pragma unroll
   for (int i = 0; i < kPeakChains; ++i) a[i] = 1e-3f * (float)((threadIdx.x + i) & 15);
-  __syncthreads();
-  const long long t0 = clock64();
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
     for (int i = 0; i < kPeakChains; ++i) a[i] = fmaf(a[i], 0.9999f, 1e-4f);
   }
-  __syncthreads();
-  const long long t1 = clock64();
   float s = 0.0f;
 #pragma unroll
   for (int i = 0; i < kPeakChains; ++i) s += a[i];
   if (s == 12345.678f) sink[blockIdx.x] = s;   // keeps the chains live; never true
-  if (threadIdx.x == 0 && blockIdx.x == 0) *cycles = t1 - t0;
 }
 
 }  // namespace
@@ -47,27 +42,23 @@ extern "C" mg_status mg_ffma_peak(double* tflops, double* flop_per_clk_per_sm, m
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   float* sink = nullptr;
-  long long* cyc = nullptr;
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
-  if (e == cudaSuccess) e = cudaMalloc(&sink, (size_t)sms * 2 * sizeof(float) + 64);
-  if (e == cudaSuccess) cyc = reinterpret_cast<long long*>(sink + sms * 2 + 8);
+  if (e == cudaSuccess) e = cudaMalloc(&sink, (size_t)sms * 2 * sizeof(float));
   if (e == cudaSuccess) e = cudaEventCreate(&ev0);
   if (e == cudaSuccess) e = cudaEventCreate(&ev1);
   const int iters = 1 << 14;
   const int grid = 2 * sms;
   float ms = 0.0f;
-  long long c = 0;
   cudaStream_t s = (cudaStream_t)stream;
   if (e == cudaSuccess) {
-    ffma_peak_kernel<<<grid, kPeakThreads, 0, s>>>(sink, iters, cyc);   // warm-up
+    ffma_peak_kernel<<<grid, kPeakThreads, 0, s>>>(sink, iters);   // warm-up
     cudaEventRecord(ev0, s);
-    ffma_peak_kernel<<<grid, kPeakThreads, 0, s>>>(sink, iters, cyc);
+    ffma_peak_kernel<<<grid, kPeakThreads, 0, s>>>(sink, iters);
     cudaEventRecord(ev1, s);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaEventSynchronize(ev1);
   if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev0, ev1);
-  if (e == cudaSuccess) e = cudaMemcpy(&c, cyc, sizeof c, cudaMemcpyDeviceToHost);
   if (ev0) cudaEventDestroy(ev0);
   if (ev1) cudaEventDestroy(ev1);
   if (sink) cudaFree(sink);
@@ -79,7 +70,16 @@ extern "C" mg_status mg_ffma_peak(double* tflops, double* flop_per_clk_per_sm, m
   }
   const double flop = 2.0 * kPeakChains * (double)iters * kPeakThreads * grid;
   *tflops = flop / (ms * 1e-3) / 1e12;
-  // block 0 shares its SM with one other block for the whole run
-  if (flop_per_clk_per_sm) *flop_per_clk_per_sm = 2.0 * 2.0 * kPeakChains * iters * kPeakThreads / (double)c;
+  if (flop_per_clk_per_sm) {
+    // per SM and clock at the device's maximum SM clock (the kernel's blocks
+    // do not all overlap on an SM, so per-block cycle counts cannot give it)
+    int khz = 0;
+    if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) {
+      cudaGetLastError();
+      *flop_per_clk_per_sm = 0.0;
+    } else {
+      *flop_per_clk_per_sm = *tflops * 1e12 / ((double)sms * khz * 1e3);
+    }
+  }
   return MG_OK;
 }

@@ -39,3 +39,15 @@ def test_loss_async_matches_loss(precision):
         assert float(host[t - 1, 0]) == plan.loss(stream)
     assert host.view(torch.int32)[:, 1].tolist() == [0, 0, 0]
     assert np.all(np.isfinite(host[:, 0].numpy()))
+
+
+def test_ffma_peak_is_the_fp32_pipe():
+    """mg_ffma_peak measures what the SMs' FP32 units can do: per SM and clock
+    (at the maximum clock) at most 128 lanes x 2 flop, and at least half of
+    it (eight independent chains per thread, two 1024-thread blocks per SM,
+    leave no latency exposed); repeated calls agree within 5%."""
+    from static_graph_nn_gb300 import binding
+    t1, per_clk = binding.ffma_peak()
+    t2, _ = binding.ffma_peak()
+    assert 128.0 <= per_clk <= 256.0 * 1.02, per_clk
+    assert abs(t1 - t2) <= 0.05 * max(t1, t2), (t1, t2)
